@@ -1,0 +1,218 @@
+// C ABI of libep_gb300 (declared in include/ep.h): host-side argument checks,
+// then kernel launches on the caller's stream.  Nothing here allocates,
+// synchronises or reads device memory.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/ep.h"
+#include "ep_kernels.cuh"
+
+namespace ep {
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_last_error[256] = {0};
+std::atomic<int> g_sm_count[64];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+ep_status_t cuda_status(cudaError_t err) {
+    if (err == cudaSuccess) return EP_OK;
+    std::strncpy(g_last_error, cudaGetErrorString(err), sizeof(g_last_error) - 1);
+    g_last_error[sizeof(g_last_error) - 1] = 0;
+    return EP_ERR_CUDA;
+}
+
+// Shared limits of every entry point.
+ep_status_t check_sizes(int32_t N, int32_t E, int32_t K) {
+    if (N < 0 || E < 1 || K < 1) return EP_ERR_INVALID_ARG;
+    if (K > E) return EP_ERR_INVALID_ARG;
+    if (E > kMaxE || K > kMaxK) return EP_ERR_UNSUPPORTED;
+    if ((int64_t)N * K > INT32_MAX) return EP_ERR_UNSUPPORTED;
+    return EP_OK;
+}
+}  // namespace
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace ep
+
+using namespace ep;
+
+extern "C" {
+
+ep_status_t ep_route_topk(const float* logits, int32_t N, int32_t E, int32_t K,
+                          const int32_t* expert_map, int32_t* topk_idx, float* topk_w,
+                          void* stream) {
+    ep_status_t st = check_sizes(N, E, K);
+    if (st != EP_OK) return st;
+    if (N > 0 && (!logits || !topk_idx || !topk_w)) return EP_ERR_INVALID_ARG;
+    if (!aligned4(logits) || !aligned4(topk_idx) || !aligned4(topk_w) || !aligned4(expert_map))
+        return EP_ERR_INVALID_ARG;
+    return cuda_status(launch_route_topk(logits, N, E, K, expert_map, topk_idx, topk_w,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+ep_status_t ep_expert_balance_map(const int32_t* counts, int32_t R, int32_t E,
+                                  int32_t* expert_map, void* stream) {
+    if (R < 1 || E < 1 || !counts || !expert_map) return EP_ERR_INVALID_ARG;
+    if (R > kMaxR || E > kMaxE) return EP_ERR_UNSUPPORTED;
+    if (E % R != 0) return EP_ERR_INVALID_ARG;
+    if (!aligned4(counts) || !aligned4(expert_map)) return EP_ERR_INVALID_ARG;
+    return cuda_status(launch_balance_map(counts, R, E, expert_map,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+size_t ep_dispatch_layout_workspace_size(int32_t N, int32_t E, int32_t K, int32_t R) {
+    if (N < 0) N = 0;
+    if (E < 1) E = 1;
+    if (R < 1) R = 1;
+    return layout_workspace_bytes(N, E, K, R);
+}
+
+ep_status_t ep_dispatch_layout(const int32_t* topk_idx, const int32_t* rank_offsets,
+                               int32_t R, int32_t N, int32_t E, int32_t K, int32_t cap,
+                               int32_t* counts, int32_t* expert_offsets,
+                               int32_t* rank_expert_offsets, int32_t* pos, int32_t* row_src,
+                               int32_t* masked_m, int32_t* overflow_count,
+                               void* workspace, size_t ws_bytes, void* stream) {
+    ep_status_t st = check_sizes(N, E, K);
+    if (st != EP_OK) return st;
+    if (R < 1) return EP_ERR_INVALID_ARG;
+    if (R > kMaxR) return EP_ERR_UNSUPPORTED;
+    if (cap < 0) return EP_ERR_INVALID_ARG;
+    if ((masked_m || overflow_count) && cap == 0) return EP_ERR_INVALID_ARG;
+    if (!rank_offsets || !counts || !expert_offsets || !rank_expert_offsets)
+        return EP_ERR_INVALID_ARG;
+    if (N > 0 && (!topk_idx || !pos || !row_src)) return EP_ERR_INVALID_ARG;
+    const void* ptrs[] = {topk_idx, rank_offsets, counts, expert_offsets, rank_expert_offsets,
+                          pos, row_src, masked_m, overflow_count};
+    for (const void* p : ptrs)
+        if (!aligned4(p)) return EP_ERR_INVALID_ARG;
+    const size_t need = layout_workspace_bytes(N, E, K, R);
+    if (!workspace || ws_bytes < need || !aligned16(workspace)) return EP_ERR_WORKSPACE;
+    LayoutArgs a;
+    a.topk_idx = topk_idx;
+    a.rank_offsets = rank_offsets;
+    a.R = R;
+    a.N = N;
+    a.E = E;
+    a.K = K;
+    a.cap = cap;
+    a.counts = counts;
+    a.expert_offsets = expert_offsets;
+    a.rank_expert_offsets = rank_expert_offsets;
+    a.pos = pos;
+    a.row_src = row_src;
+    a.masked_m = masked_m;
+    a.overflow = overflow_count;
+    a.ws_hist = static_cast<int32_t*>(workspace);
+    a.ws_totals = a.ws_hist + (size_t)layout_chunk_slots(N, R) * E;
+    return cuda_status(launch_layout(a, static_cast<cudaStream_t>(stream)));
+}
+
+static ep_status_t check_move(const void* src, int32_t N, int32_t H, int32_t E, int32_t K,
+                              const int32_t* topk_idx, const int32_t* pos,
+                              const int32_t* expert_offsets, ep_layout_t layout, int32_t cap,
+                              const void* dst) {
+    ep_status_t st = check_sizes(N, E, K);
+    if (st != EP_OK) return st;
+    if (H < 8 || H % 8 != 0) return EP_ERR_INVALID_ARG;
+    if (layout != EP_LAYOUT_CONTIG && layout != EP_LAYOUT_MASKED) return EP_ERR_INVALID_ARG;
+    if (layout == EP_LAYOUT_MASKED && cap < 1) return EP_ERR_INVALID_ARG;
+    if (N > 0 && (!src || !topk_idx || !pos || !dst)) return EP_ERR_INVALID_ARG;
+    if (N > 0 && layout == EP_LAYOUT_MASKED && !expert_offsets) return EP_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return EP_ERR_INVALID_ARG;
+    if (!aligned4(topk_idx) || !aligned4(pos) || !aligned4(expert_offsets))
+        return EP_ERR_INVALID_ARG;
+    return EP_OK;
+}
+
+ep_status_t ep_dispatch(const void* x, int32_t N, int32_t H, int32_t E, int32_t K,
+                        const int32_t* topk_idx, const int32_t* pos,
+                        const int32_t* expert_offsets, ep_layout_t layout, int32_t cap,
+                        ep_dtype_t dtype, void* out, float* out_scales, void* stream) {
+    ep_status_t st = check_move(x, N, H, E, K, topk_idx, pos, expert_offsets, layout, cap, out);
+    if (st != EP_OK) return st;
+    if (dtype != EP_DTYPE_BF16 && dtype != EP_DTYPE_FP8_E4M3_B128) return EP_ERR_INVALID_ARG;
+    if (dtype == EP_DTYPE_FP8_E4M3_B128) {
+        if (H % 128 != 0) return EP_ERR_INVALID_ARG;
+        if (N > 0 && !out_scales) return EP_ERR_INVALID_ARG;
+        if (!aligned4(out_scales)) return EP_ERR_INVALID_ARG;
+    }
+    MoveArgs a;
+    a.src = x;
+    a.dst = out;
+    a.scales = out_scales;
+    a.topk_idx = topk_idx;
+    a.topk_w = nullptr;
+    a.pos = pos;
+    a.expert_offsets = expert_offsets;
+    a.N = N;
+    a.H = H;
+    a.E = E;
+    a.K = K;
+    a.cap = cap;
+    a.layout = (int)layout;
+    a.dtype = (int)dtype;
+    return cuda_status(launch_dispatch(a, static_cast<cudaStream_t>(stream)));
+}
+
+ep_status_t ep_combine(const void* y, int32_t N, int32_t H, int32_t E, int32_t K,
+                       const int32_t* topk_idx, const float* topk_w, const int32_t* pos,
+                       const int32_t* expert_offsets, ep_layout_t layout, int32_t cap,
+                       void* out, void* stream) {
+    ep_status_t st = check_move(y, N, H, E, K, topk_idx, pos, expert_offsets, layout, cap, out);
+    if (st != EP_OK) return st;
+    if (N > 0 && !topk_w) return EP_ERR_INVALID_ARG;
+    if (!aligned4(topk_w)) return EP_ERR_INVALID_ARG;
+    MoveArgs a;
+    a.src = y;
+    a.dst = out;
+    a.scales = nullptr;
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    a.pos = pos;
+    a.expert_offsets = expert_offsets;
+    a.N = N;
+    a.H = H;
+    a.E = E;
+    a.K = K;
+    a.cap = cap;
+    a.layout = (int)layout;
+    a.dtype = 0;
+    return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
+}
+
+const char* ep_status_string(ep_status_t status) {
+    switch (status) {
+        case EP_OK: return "EP_OK";
+        case EP_ERR_INVALID_ARG: return "EP_ERR_INVALID_ARG";
+        case EP_ERR_WORKSPACE: return "EP_ERR_WORKSPACE";
+        case EP_ERR_CUDA: return "EP_ERR_CUDA";
+        case EP_ERR_UNSUPPORTED: return "EP_ERR_UNSUPPORTED";
+    }
+    return "EP_ERR_UNKNOWN";
+}
+
+const char* ep_last_cuda_error(void) { return g_last_error; }
+
+uint64_t ep_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int32_t ep_abi_version(void) { return 1; }
+
+}  // extern "C"

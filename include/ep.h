@@ -1,0 +1,212 @@
+/*
+ * ep.h -- C ABI of libep_gb300: the MoE expert-parallel hot path
+ * (route top-K -> layout -> dispatch -> combine) on one GB300 (sm_103a).
+ *
+ * Expert parallelism with data-parallel attention is emulated on one GPU: R
+ * logical data-parallel ranks hold B_i tokens each, packed rank-major in one
+ * buffer (token t of rank r is row rank_offsets[r] + i).  Experts are split
+ * into R contiguous sets of E/R; the all-to-all of a multi-GPU system becomes
+ * the HBM scatter (dispatch) and gather (combine) below.
+ *
+ * Sources, by page title and section:
+ *   [Anatomy]  "Anatomy of a High-Performance EP Kernel" (Korean and Chinese
+ *              renderings): "What we have to do" (shapes (B_i,H), (B_i,E),
+ *              (B_i,K); routing table t0..t3), "High throughput: ask first,
+ *              then send", "Dispatch" (dense per-expert buffer for the
+ *              grouped GEMM; irregular per-expert counts).
+ *   [Moreh]    "21K output tokens/s DeepSeek inference on AMD Instinct MI300X
+ *              GPUs with Expert Parallelism": "Parallelization method"
+ *              (DP8/EP8, 32 of 256 experts per GPU), "Load balancing across
+ *              GPUs" (balanced expert renumbering), "Using HIP Graphs"
+ *              (static tensor sizes for graph capture).
+ *   [SGLang]   "Expert Parallelism" (SGLang docs): "Backends for MoE
+ *              computation" (deep_gemm: contiguous layout for prefill, masked
+ *              layout for decode, FP8 block-wise quantisation), "Supported
+ *              backends" (normal vs low_latency / CUDA-graph-compatible
+ *              modes), "Framework overview" (TopK -> dispatch -> runner ->
+ *              combine -> final_hidden_states).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are device pointers owned by the caller unless stated; the
+ *     library allocates and frees nothing, and keeps no pointer after return.
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
+ *     the legacy default stream) and returns without synchronising; no call
+ *     reads device memory on the host, so every call can be captured in a
+ *     CUDA graph.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns EP_ERR_INVALID_ARG (or EP_ERR_WORKSPACE /
+ *     EP_ERR_UNSUPPORTED) and launches nothing.  A failed launch returns
+ *     EP_ERR_CUDA.  No kernel traps, asserts or waits on another kernel.
+ *   - Device-side data that break a precondition (an expert id outside
+ *     [0,E), rank_offsets that are not a non-decreasing 0..N sequence, pos
+ *     values that do not come from ep_dispatch_layout) never cause an access
+ *     outside the buffers described here: such picks are skipped.
+ *   - bf16 is IEEE binary16-brain (1-8-7); FP8 is OCP E4M3FN.
+ *   - Limits: 1 <= E <= 1024, 1 <= K <= min(E, 32), 1 <= R <= 1024,
+ *     0 <= N, N*K <= 2^31 - 1; beyond them EP_ERR_UNSUPPORTED.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1,  /* null pointer, bad size or alignment */
+    EP_ERR_WORKSPACE = 2,    /* workspace missing or smaller than required */
+    EP_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    EP_ERR_UNSUPPORTED = 4   /* sizes beyond the documented limits */
+} ep_status_t;
+
+typedef enum {
+    EP_LAYOUT_CONTIG = 0,    /* [N*K, H] rows grouped by expert (prefill) */
+    EP_LAYOUT_MASKED = 1     /* [E, cap, H] fixed capacity per expert (decode) */
+} ep_layout_t;
+
+typedef enum {
+    EP_DTYPE_BF16 = 0,          /* rows copied as bf16 */
+    EP_DTYPE_FP8_E4M3_B128 = 1  /* E4M3 codes + one float scale per 128 columns */
+} ep_dtype_t;
+
+/*
+ * ep_route_topk -- [Anatomy] "What we have to do": each token's router
+ * logits (length E) select the K experts with the largest logits, giving the
+ * (B_i, K) assignment (the table's t0 row routes to [3, 13]).
+ *   logits     float32 [N, E] row-major, finite values (NaN is not ordered).
+ *   expert_map int32 [E] or NULL; when given, output ids are expert_map[id]
+ *              ([Moreh] "Load balancing across GPUs": the gate must emit the
+ *              renumbered ids).  Entries outside [0,E) become "no pick".
+ *   topk_idx   int32 [N, K] out: picks in descending logit order; equal
+ *              logits go to the lower expert id; -0.0 equals +0.0.
+ *   topk_w     float32 [N, K] out: softmax over the K picked logits,
+ *              w_k = exp(l_k - l_0) / sum_j exp(l_j - l_0), in float (the
+ *              pages print no gate formula; softmax renormalised over the
+ *              top K is the reading used).
+ */
+ep_status_t ep_route_topk(const float* logits, int32_t N, int32_t E, int32_t K,
+                          const int32_t* expert_map, int32_t* topk_idx, float* topk_w,
+                          void* stream);
+
+/*
+ * ep_expert_balance_map -- [Moreh] "Load balancing across GPUs": group the E
+ * experts into R sets of E/R with balanced activation frequency and renumber
+ * each set contiguously.  The page names the problem (a balanced number
+ * partitioning variant) but no algorithm; this computes the greedy one:
+ * frequency[e] = sum_r counts[r][e]; experts in descending frequency (ties:
+ * lower id) each join the set with the least load among sets with room
+ * (ties: lower set id); new id = set * (E/R) + arrival order in the set.
+ *   counts     int32 [R, E] per-(rank, expert) counts (ep_dispatch_layout's
+ *              output for a calibration batch), non-negative.
+ *   expert_map int32 [E] out: old id -> new id, a permutation of [0, E).
+ * Requires E % R == 0.  One small single-block kernel.
+ */
+ep_status_t ep_expert_balance_map(const int32_t* counts, int32_t R, int32_t E,
+                                  int32_t* expert_map, void* stream);
+
+/*
+ * Bytes of device workspace ep_dispatch_layout needs for these sizes (a
+ * multiple of 256; 0 never occurs).  Pure host function.
+ */
+size_t ep_dispatch_layout_workspace_size(int32_t N, int32_t E, int32_t K, int32_t R);
+
+/*
+ * ep_dispatch_layout -- [Anatomy] "High throughput: ask first, then send":
+ * every (rank, expert) count is known before any row moves, and each expert's
+ * rows form one dense block for the grouped GEMM ("Dispatch").  A stable
+ * counting sort of the N*K picks by expert id:
+ *   topk_idx            int32 [N, K]; ids outside [0,E) are "no pick".
+ *   rank_offsets        int32 [R+1] device: 0 = o_0 <= o_1 <= ... <= o_R = N;
+ *                       tokens [o_r, o_{r+1}) belong to rank r.
+ *   cap                 0, or the masked capacity per expert (> 0).
+ *   counts              int32 [R, E] out: picks of expert e by rank r.
+ *   expert_offsets      int32 [E+1] out: exclusive prefix of expert totals;
+ *                       expert_offsets[E] = number of valid picks.
+ *   rank_expert_offsets int32 [R, E] out: expert_offsets[e] +
+ *                       sum_{r'<r} counts[r'][e] (where rank r's rows for
+ *                       expert e start).
+ *   pos                 int32 [N, K] out: row of pick (t,k) in the expert-
+ *                       major buffer; within an expert, picks keep (t, k)
+ *                       order (hence source-rank order); -1 for no pick.
+ *   row_src             int32 [N*K] out: token of row p; -1 past the valid
+ *                       rows.
+ *   masked_m            int32 [E] or NULL out (needs cap > 0): min(total, cap)
+ *                       ([SGLang] masked layout's per-expert valid count).
+ *   overflow_count      int32 [1] or NULL out (needs cap > 0): picks beyond
+ *                       cap, which the masked layout drops.
+ *   workspace           device scratch of ws_bytes >= the size above; its
+ *                       contents need no initialisation and are clobbered.
+ * Three kernels; results are deterministic (no order depends on atomics).
+ */
+ep_status_t ep_dispatch_layout(const int32_t* topk_idx, const int32_t* rank_offsets,
+                               int32_t R, int32_t N, int32_t E, int32_t K, int32_t cap,
+                               int32_t* counts, int32_t* expert_offsets,
+                               int32_t* rank_expert_offsets, int32_t* pos, int32_t* row_src,
+                               int32_t* masked_m, int32_t* overflow_count,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * ep_dispatch -- [Anatomy] "Dispatch" and [SGLang] deep_gemm row: scatter each
+ * token's activation row to the rows of its K picks.  Each source row is read
+ * once and written K times.
+ *   x              bf16 [N, H], 16-byte aligned; H % 8 == 0.
+ *   topk_idx, pos, expert_offsets: as produced by ep_dispatch_layout.
+ *   layout CONTIG: out rows = N*K, row of pick (t,k) = pos[t,k].
+ *   layout MASKED: out is [E, cap, H]; slot = pos[t,k] - expert_offsets[e];
+ *                  delivered to (e, slot) when slot < cap, else dropped.
+ *                  Rows at or past masked_m[e] are not written.
+ *   dtype BF16:    out bf16 rows, bit copies of x; out_scales unused (NULL ok).
+ *   dtype FP8_E4M3_B128 ([SGLang] "FP8 block-wise quantisation"; block size
+ *                  1x128 and E4M3 are the reading used): H % 128 == 0; per
+ *                  token and 128-column block b, amax = max|x|, scale =
+ *                  amax / 448 (IEEE float division; 1 when amax == 0), code =
+ *                  E4M3(x / scale) rounded to nearest even with saturation to
+ *                  +-448; out uint8 codes [rows, H], out_scales float32
+ *                  [rows, H/128].  The codes are computed once per token and
+ *                  written to all K rows.
+ *   out            16-byte aligned.
+ */
+ep_status_t ep_dispatch(const void* x, int32_t N, int32_t H, int32_t E, int32_t K,
+                        const int32_t* topk_idx, const int32_t* pos,
+                        const int32_t* expert_offsets, ep_layout_t layout, int32_t cap,
+                        ep_dtype_t dtype, void* out, float* out_scales, void* stream);
+
+/*
+ * ep_combine -- [Anatomy] "bring the results home" after the expert GEMM, and
+ * [SGLang] "Framework overview" (Dispatcher.combine -> final_hidden_states):
+ *   out[t] = bf16_rn( sum_{k=0..K-1} topk_w[t,k] * y[row(t,k)] )
+ * accumulated in float, one fused multiply-add per pick in the order k = 0..
+ * K-1; picks that were not delivered (no pick, masked overflow) add nothing.
+ *   y      bf16 expert outputs, 16-byte aligned: [N*K, H] (CONTIG) or
+ *          [E, cap, H] (MASKED); row(t,k) as in ep_dispatch.
+ *   topk_w float32 [N, K].
+ *   out    bf16 [N, H], 16-byte aligned; must not overlap y.
+ */
+ep_status_t ep_combine(const void* y, int32_t N, int32_t H, int32_t E, int32_t K,
+                       const int32_t* topk_idx, const float* topk_w, const int32_t* pos,
+                       const int32_t* expert_offsets, ep_layout_t layout, int32_t cap,
+                       void* out, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* ep_status_string(ep_status_t status);
+
+/* Text of the last CUDA error seen by this library on the calling thread
+ * ("" if none); valid until the next call on that thread. */
+const char* ep_last_cuda_error(void);
+
+/* Number of kernels this library has launched in this process (all threads,
+ * all devices).  Lets a caller count launches inside a timed region. */
+uint64_t ep_kernel_launch_count(void);
+
+/* ABI version of this header: 1. */
+int32_t ep_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_H */

@@ -1,0 +1,107 @@
+"""The C ABI library: it loads, exports every function include/ep.h declares,
+and its host-side argument checks return the documented status codes without
+launching anything (these calls never reach the GPU, so they run on CPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from combine_ep_route_topk_gb300 import build as ep_build
+from combine_ep_route_topk_gb300 import ep
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, WORKSPACE, CUDA, UNSUPPORTED = 0, 1, 2, 3, 4
+P = ctypes.c_void_p
+
+
+@pytest.fixture(scope="module")
+def L():
+    ep_build.build()
+    return ep.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ep.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ep_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared()
+    assert "ep_route_topk" in names and "ep_combine" in names and len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_static_queries(L):
+    assert L.ep_abi_version() == 1
+    assert L.ep_status_string(0) == b"EP_OK"
+    assert L.ep_status_string(2) == b"EP_ERR_WORKSPACE"
+    assert L.ep_kernel_launch_count() == 0
+    a = ep.ep_dispatch_layout_workspace_size(32768, 256, 8, 8)
+    b = ep.ep_dispatch_layout_workspace_size(65536, 256, 8, 8)
+    assert a % 256 == 0 and b % 256 == 0 and 0 < a <= b
+
+
+def p(v=4096):
+    return P(v)
+
+
+def test_route_argument_checks(L):
+    f = L.ep_route_topk
+    assert f(p(), 10, 16, 17, None, p(), p(), None) == INVALID       # K > E
+    assert f(p(), 10, 16, 0, None, p(), p(), None) == INVALID        # K < 1
+    assert f(p(), -1, 16, 2, None, p(), p(), None) == INVALID        # N < 0
+    assert f(p(), 10, 2048, 2, None, p(), p(), None) == UNSUPPORTED  # E > 1024
+    assert f(p(), 10, 64, 33, None, p(), p(), None) == UNSUPPORTED   # K > 32
+    assert f(p(), 1 << 30, 16, 4, None, p(), p(), None) == UNSUPPORTED  # N*K overflow
+    assert f(None, 10, 16, 2, None, p(), p(), None) == INVALID       # null logits
+    assert f(p(4098), 10, 16, 2, None, p(), p(), None) == INVALID    # misaligned
+    assert L.ep_kernel_launch_count() == 0
+
+
+def test_layout_argument_checks(L):
+    f = L.ep_dispatch_layout
+    need = ep.ep_dispatch_layout_workspace_size(100, 16, 2, 4)
+
+    def call(R=4, N=100, E=16, K=2, cap=0, mm=None, ov=None, ws=p(), wsb=need):
+        return f(p(), p(), R, N, E, K, cap, p(), p(), p(), p(), p(), mm, ov, ws, wsb, None)
+    assert call(wsb=need - 1) == WORKSPACE
+    assert call(ws=None) == WORKSPACE
+    assert call(ws=p(4104)) == WORKSPACE  # workspace not 16-byte aligned
+    assert call(R=0) == INVALID
+    assert call(R=2000) == UNSUPPORTED
+    assert call(cap=-1) == INVALID
+    assert call(cap=0, mm=p()) == INVALID  # masked outputs need a capacity
+    assert call(K=20) == INVALID
+    assert L.ep_kernel_launch_count() == 0
+
+
+def test_dispatch_and_combine_argument_checks(L):
+    d = L.ep_dispatch
+    c = L.ep_combine
+
+    def disp(x=p(), H=1024, layout=0, cap=0, dtype=0, scales=None, out=p()):
+        return d(x, 100, H, 16, 2, p(), p(), p(), layout, cap, dtype, out, scales, None)
+    assert disp(H=100) == INVALID                 # H % 8
+    assert disp(H=0) == INVALID
+    assert disp(x=p(4104)) == INVALID             # x not 16-byte aligned
+    assert disp(out=p(4100)) == INVALID           # out not 16-byte aligned
+    assert disp(layout=1, cap=0) == INVALID       # masked needs cap > 0
+    assert disp(layout=7) == INVALID
+    assert disp(dtype=9) == INVALID
+    assert disp(dtype=1, H=520, scales=p()) == INVALID  # FP8 needs H % 128
+    assert disp(dtype=1, scales=None) == INVALID        # FP8 needs scales
+    assert c(p(), 100, 1024, 16, 2, p(), None, p(), p(), 0, 0, p(), None) == INVALID  # no weights
+    assert c(p(), 100, 1024, 16, 20, p(), p(), p(), p(), 0, 0, p(), None) == INVALID  # K > E
+    assert L.ep_expert_balance_map(p(), 3, 16, p(), None) == INVALID  # E % R != 0
+    assert L.ep_expert_balance_map(p(), 0, 16, p(), None) == INVALID
+    assert L.ep_kernel_launch_count() == 0
+
+
+def test_binding_refuses_cpu_tensors(L):
+    import torch
+    with pytest.raises(ep.EPError):
+        ep.ep_route_topk(torch.zeros(4, 16), 2, topk_idx=torch.zeros(4, 2, dtype=torch.int32),
+                         topk_w=torch.zeros(4, 2))
