@@ -1,0 +1,454 @@
+"""Benchmark: MoE expert-parallel route -> layout -> dispatch -> combine on GB300.
+
+One step = one pass of the whole hot path over one batch of the prefill
+workload: 8 logical data-parallel ranks x 4096 tokens (N = 32768), E = 256
+experts, K = 8, H = 7168; route top-K over float32 logits, stable expert-major
+layout, FP8 E4M3 1x128 contiguous dispatch, combine of bf16 expert outputs
+(the stand-in for the grouped GEMM, N(0,1)) with fp32 accumulation.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  `value` is whole-path tokens/s with inputs
+resident in HBM (per-step CUDA events on the launching stream, L2 flushed
+between steps with a 512 MiB write); `e2e` times the same path through the
+public API with pinned host buffers, host->device copies of the step's inputs
+and the device->host read of the combined output inside the timed region.
+`--impl reference` times the CPU oracle (single thread) on a bounded sample
+of the same workload.  With N > 1 (torchrun) each rank runs an independent
+replica of the path on its own GPU and batch (weak scaling; there is no data
+exchange between ranks, only a host barrier and a max-reduction of times).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak) on 1 GB300"
+SPEC_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD_DESC = ("prefill: 8 logical ranks x 4096 tokens (N=32768), E=256 experts (32/rank), "
+                 "K=8, H=7168; FP8 E4M3 1x128 contiguous dispatch; combine of bf16 expert "
+                 "outputs N(0,1), fp32 accumulate")
+
+
+# ------------------------------------------------------------------ helpers --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    # host-side barrier and max-reduction only: gloo, no GPU collective
+    dist.init_process_group("gloo")
+    return dist
+
+
+def max_over_ranks(dist, value: float) -> float:
+    """Largest value over all ranks (the slowest rank sets the job time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "combine_ep_route_topk_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, src_files):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash(src_files):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms={period_ms}", f"--id={gpu_id}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_smi_id(local: int) -> str:
+    """nvidia-smi --id for this process's CUDA device (its UUID when known)."""
+    import torch
+    uuid = getattr(torch.cuda.get_device_properties(local), "uuid", None)
+    if uuid:
+        u = str(uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        parts = [p.strip() for p in vis.split(",") if p.strip()]
+        if local < len(parts):
+            return parts[local]
+    return str(local)
+
+
+def byte_model(N, E, K, H):
+    """Algorithmic bytes per launch (the minimum each kernel must move)."""
+    sb = H // 128 * 4
+    return {
+        "route": N * E * 4 + N * K * 8,
+        "layout": N * K * 4 + N * K * 8,
+        "dispatch": N * H * 2 + N * K * (H + sb) + N * K * 8,
+        "combine": N * K * H * 2 + N * H * 2 + N * K * 12,
+        # each pick counted as a full row read and a row written
+        "dispatch_rowwise": N * K * H * 2 + N * K * (H + sb),
+    }
+
+
+# ------------------------------------------------------------------ our arm --
+
+def run_ours(args, world, rank, local):
+    import torch
+    import combine_ep_route_topk_gb300 as ep
+    from combine_ep_route_topk_gb300 import workloads as wl
+
+    dist = init_dist(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.WORKLOADS["prefill"]
+    if args.tokens_per_rank:  # smaller case of the same workload (profiling)
+        w = w.scaled(batch=("fixed", args.tokens_per_rank))
+    inp = wl.make_inputs(w, seed=args.seed + rank, device=str(dev))
+    N, E, K, H, R = inp["N"], w.E, w.K, w.H, w.R
+    logits, ro, x, y = inp["logits"], inp["rank_offsets"], inp["x"], inp["y"]
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    idx = torch.empty(N, K, dtype=torch.int32, device=dev)
+    wt = torch.empty(N, K, dtype=torch.float32, device=dev)
+    lay = ep.alloc_layout(N, E, K, R, 0, dev)
+    ws = torch.empty(ep.ep_dispatch_layout_workspace_size(N, E, K, R), dtype=torch.uint8,
+                     device=dev)
+    q = torch.empty(N * K, H, dtype=torch.uint8, device=dev)
+    qs = torch.empty(N * K, H // 128, dtype=torch.float32, device=dev)
+    comb = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        ep.ep_route_topk(logits, K, topk_idx=idx, topk_w=wt)
+        if ev:
+            ev[1].record(stream)
+        ep.ep_dispatch_layout(idx, ro, E, 0, out=lay, workspace=ws)
+        if ev:
+            ev[2].record(stream)
+        ep.ep_dispatch(x, idx, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_CONTIG, 0,
+                       ep.EP_DTYPE_FP8_E4M3_B128, out=q, out_scales=qs)
+        if ev:
+            ev[3].record(stream)
+        ep.ep_combine(y, idx, wt, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_CONTIG, 0,
+                      out=comb)
+        if ev:
+            ev[4].record(stream)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_smi_id(local)) if rank == 0 else None
+    barrier(dist)
+    torch.cuda.synchronize()
+    launches0 = ep.ep_kernel_launch_count()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_((i + 7) & 0xFF)  # L2 flush, outside the step's events
+        step(evs[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    barrier(dist)
+    launches = ep.ep_kernel_launch_count() - launches0
+    clocks = sampler.stop() if sampler else None
+
+    stage = {n: [e[j].elapsed_time(e[j + 1]) for e in evs]
+             for j, n in enumerate(["route", "layout", "dispatch", "combine"])}
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    total_ms = max_over_ranks(dist, sum(step_ms))
+    dc_ms = max_over_ranks(dist, sum(a + b for a, b in zip(stage["dispatch"], stage["combine"])))
+
+    # ---- end to end through the public API, host buffers --------------------
+    e2e_steps = min(args.steps, 10)
+    def pinned_copy(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+    x_h, lg_h, ro_h, y_h = (pinned_copy(t) for t in (x, logits, ro, y))
+    out_h = torch.empty(N, H, dtype=torch.bfloat16).pin_memory()
+    h2d = x_h.numel() * 2 + lg_h.numel() * 4 + ro_h.numel() * 4 + y_h.numel() * 2
+    d2h = out_h.numel() * 2
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(e2e_steps + 1)]
+    barrier(dist)
+    for i in range(e2e_steps + 1):  # the first pass is a warm-up
+        a, b = e2e_ev[i]
+        a.record(stream)
+        x.copy_(x_h, non_blocking=True)
+        logits.copy_(lg_h, non_blocking=True)
+        ro.copy_(ro_h, non_blocking=True)
+        y.copy_(y_h, non_blocking=True)
+        step()
+        out_h.copy_(comb, non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    e2e_ms = max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in e2e_ev[1:]))
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return None
+
+    steps = args.steps
+    tok = N * world
+    ms_per_step = total_ms / steps
+    value = tok * steps / (total_ms / 1e3)
+    bm = byte_model(N, E, K, H)
+    peak, peak_kind = measured_peaks()
+    mean = {k: statistics.fmean(v) for k, v in stage.items()}
+    kernels = {}
+    for k in ["route", "layout", "dispatch", "combine"]:
+        gbs = bm[k] / (mean[k] / 1e3) / 1e9
+        kernels[k] = {"ms": round(mean[k], 4), "bytes": bm[k], "GB/s": round(gbs, 1),
+                      "frac_of_measured": round(gbs / peak, 4),
+                      "frac_of_8TBs": round(gbs / SPEC_HBM_GBS, 4)}
+    kernels["dispatch"]["GB/s_rowwise_accounting"] = round(
+        bm["dispatch_rowwise"] / (mean["dispatch"] / 1e3) / 1e9, 1)
+    dc_bytes = bm["dispatch"] + bm["combine"]
+    dc_per = dc_ms / steps
+    comb_gbs = bm["combine"] / (mean["combine"] / 1e3) / 1e9
+    traffic = ncu_traffic("combine", ["combine.cu"])
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC if not args.tokens_per_rank else
+                   f"prefill shape at 8 ranks x {args.tokens_per_rank} tokens",
+                   "R": w.R, "N": N, "E": E, "K": K, "H": H,
+                   "layout": "contiguous", "dispatch_dtype": "fp8_e4m3_1x128",
+                   "step": "route+layout+dispatch+combine",
+                   "l2": "flushed between steps (512 MiB write, outside the step events); "
+                         "inputs (x 0.47 GB, y 3.76 GB) also exceed L2",
+                   "parallelism": f"{world} independent replica(s), one per GPU"},
+        "roofline": {"kernel": "combine", "bound": "hbm", "achieved": round(comb_gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(comb_gbs / peak, 4),
+                     "peak_source": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes": bm["combine"]},
+        "dispatch_combine": {"tokens_per_s": round(tok * steps / (dc_ms / 1e3), 1),
+                             "ms": round(dc_per, 4),
+                             "GB/s": round(dc_bytes / (dc_per / 1e3) / 1e9, 1),
+                             "frac_of_measured": round(dc_bytes / (dc_per / 1e3) / 1e9 / peak, 4),
+                             "frac_of_8TBs": round(dc_bytes / (dc_per / 1e3) / 1e9 / SPEC_HBM_GBS,
+                                                   4)},
+        "kernels": kernels,
+        "e2e": {"value": round(tok * e2e_steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms / e2e_steps, 3), "steps": e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if args.cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def oracle_sample(tokens_per_rank: int, seed: int):
+    """The prefill workload's recipe at a bounded size: 8 ranks x
+    tokens_per_rank tokens, same E/K/H, distributions and dtypes."""
+    import numpy as np
+    import torch
+    from combine_ep_route_topk_gb300 import workloads as wl
+    w = wl.WORKLOADS["prefill"].scaled(batch=("fixed", tokens_per_rank))
+    inp = wl.make_inputs(w, seed=seed)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    return w, dict(logits=inp["logits"].numpy(), ro=inp["rank_offsets"].numpy(),
+                   x=bits(inp["x"]), y=bits(inp["y"]), N=inp["N"])
+
+
+def oracle_step(w, s):
+    import oracle
+    idx, wt = oracle.route_topk(s["logits"], w.K)
+    lay = oracle.layout(idx, s["ro"], w.E)
+    oracle.dispatch(s["x"], idx, lay["pos"], lay["expert_offsets"], w.E,
+                    layout=oracle.LAYOUT_CONTIG, dtype=oracle.DTYPE_FP8)
+    oracle.combine(s["y"], idx, wt, lay["pos"], lay["expert_offsets"], w.E)
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    """The oracle as it stands, one thread, on sub-batches of the prefill
+    workload (8 ranks x 256 tokens each) until about budget_s of CPU work."""
+    per_rank = 256
+    w, s = oracle_sample(per_rank, seed=1000)
+    total_tok, total_s, reps = 0, 0.0, 0
+    while total_s < budget_s and reps < 64:
+        t0 = time.perf_counter()
+        oracle_step(w, s)
+        total_s += time.perf_counter() - t0
+        total_tok += s["N"]
+        reps += 1
+    return {"value": round(total_tok / total_s, 1), "unit": "tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"one sub-batch of the prefill workload (8 ranks x {per_rank} tokens, "
+                      f"E=256, K=8, H=7168; route, layout, FP8 dispatch, combine) run {reps} "
+                      f"times: {total_tok} tokens in {total_s:.1f} s, single-threaded"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    # bounded per-step sample so warm-up + steps take about 90 s of CPU
+    per_token_s = 0.6e-3
+    per_rank = int(90.0 / (per_token_s * max(1, args.steps + args.warmup)) / 8)
+    per_rank = max(4, min(512, per_rank))
+    w, s = oracle_sample(per_rank, seed=args.seed)
+    for _ in range(args.warmup):
+        oracle_step(w, s)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(w, s)
+        times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = s["N"] * args.steps / tot
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "step": "route+layout+dispatch+combine",
+                   "sample_per_step": f"8 ranks x {per_rank} tokens of the same workload"},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"each step: 8 ranks x {per_rank} tokens ({s['N']} tokens)"},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--tokens-per-rank", type=int, default=0,
+                    help="run a smaller case of the workload (default: the full 4096)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
