@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libep_gb300.so")
-SOURCES = ["ep_api.cu", "route_topk.cu", "layout.cu", "dispatch.cu", "combine.cu"]
+SOURCES = ["ep_api.cu", "route_topk.cu", "layout.cu", "layout_static.cu", "dispatch.cu",
+           "combine.cu"]
 HEADERS = [os.path.join(CSRC, "ep_kernels.cuh"), os.path.join(ROOT, "include", "ep.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

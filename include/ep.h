@@ -149,6 +149,38 @@ ep_status_t ep_dispatch_layout(const int32_t* topk_idx, const int32_t* rank_offs
                                int32_t* masked_m, int32_t* overflow_count,
                                void* workspace, size_t ws_bytes, void* stream);
 
+/* Bytes of the fixed scratch array that ep_dispatch_layout_static keeps
+ * inside the library on every GPU that loads it (4 MiB). */
+#define EP_LAYOUT_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+/*
+ * ep_dispatch_layout_static -- no counterpart in the source pages; an
+ * addition of this library for callers that cannot allocate device memory
+ * (an embedder whose device memory is reserved up front by another
+ * allocator, a plain C host without a device allocator, code running where
+ * cudaMalloc is not permitted).  Same inputs, outputs and results as
+ * ep_dispatch_layout, but no workspace argument: the scratch is a fixed
+ * array of EP_LAYOUT_STATIC_SCRATCH_BYTES inside the library, held by every
+ * GPU that loads the library until the process exits.
+ *   - Sizes whose scratch (ep_dispatch_layout_workspace_size) exceeds
+ *     EP_LAYOUT_STATIC_SCRATCH_BYTES return EP_ERR_UNSUPPORTED and launch
+ *     nothing; other argument errors as for ep_dispatch_layout.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.  A failed lookup returns EP_ERR_CUDA.
+ *   - Allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
+ *   - All calls share the array and it keeps the last call's contents; the
+ *     kernels write every entry they read, so nothing needs clearing.  Calls
+ *     that overlap on the GPU (different streams or host threads) race on
+ *     the array: order them on one stream.
+ */
+ep_status_t ep_dispatch_layout_static(const int32_t* topk_idx, const int32_t* rank_offsets,
+                                      int32_t R, int32_t N, int32_t E, int32_t K, int32_t cap,
+                                      int32_t* counts, int32_t* expert_offsets,
+                                      int32_t* rank_expert_offsets, int32_t* pos,
+                                      int32_t* row_src, int32_t* masked_m,
+                                      int32_t* overflow_count, void* stream);
+
 /*
  * ep_dispatch -- [Anatomy] "Dispatch" and [SGLang] deep_gemm row: scatter each
  * token's activation row to the rows of its K picks.  Each source row is read
