@@ -305,7 +305,8 @@ def run_ours(args, world, rank, local):
     dc_bytes = bm["dispatch"] + bm["combine"]
     dc_per = dc_ms / steps
     comb_gbs = bm["combine"] / (mean["combine"] / 1e3) / 1e9
-    traffic = ncu_traffic("combine", ["combine.cu"])
+    # the committed counters describe the full-size launch only
+    traffic = None if args.tokens_per_rank else ncu_traffic("combine", ["combine.cu"])
     line = {
         "metric": METRIC,
         "value": round(value, 1),

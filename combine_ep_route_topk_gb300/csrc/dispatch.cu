@@ -7,9 +7,9 @@
 // On one GPU the all-to-all is an HBM scatter.  One block per token reads
 // the token's row once (16-byte streaming loads, all of a thread's vectors in
 // flight before any store) and writes it to the K destination rows
-// (16-byte stores for bf16, 8-byte for FP8 codes).  The FP8 variant
-// quantises once per token: a 128-column block is 16 lanes x 8 values, its
-// amax is a 4-step shuffle reduction within the half-warp, scale = amax/448
+// (16-byte stores).  The FP8 variant quantises once per token: a 128-column
+// block is 8 lanes x 16 values, its amax a 3-step shuffle reduction within
+// the 8 lanes, scale = amax/448
 // and x/scale use IEEE division, and the E4M3 conversion is the hardware
 // round-to-nearest-even satfinite cvt.  Bytes moved per token:
 // H*2 read + K*(H*b_out + scales) written; the kernel is HBM-bound.
@@ -71,61 +71,75 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
 }
 
+// E4M3 codes of 16 values as 16 bytes (value j in byte j).
+__device__ __forceinline__ uint4 quantize16(const uint4& lo, const uint4& hi, float scale) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t p[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        p[j] = e4m3x2(__fdiv_rn(bf16_lo(w[j]), scale), __fdiv_rn(bf16_hi(w[j]), scale));
+    return make_uint4(p[0] | (p[1] << 16), p[2] | (p[3] << 16), p[4] | (p[5] << 16),
+                      p[6] | (p[7] << 16));
+}
+
+__device__ __forceinline__ float amax16(const uint4& lo, const uint4& hi) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+    return m;
+}
+
+// Each thread owns 16 consecutive values; 8 lanes make one 128-column scale
+// block.  One 16-byte code store per destination, and one scale store per
+// block and destination (lane 0 of the 8).
 template <int NT, int U>
 __global__ void __launch_bounds__(NT) dispatch_fp8_kernel(MoveArgs a) {
     __shared__ long long s_dst[kMaxK];
     const int t = blockIdx.x;
     if (threadIdx.x < a.K) s_dst[threadIdx.x] = dest_row(a, t, threadIdx.x);
     __syncthreads();
-    const int V = a.H >> 3;   // 8-value vectors per row; 16 per 128-block
+    const int G = a.H >> 4;   // 16-value groups per row; 8 per scale block
     const int SB = a.H >> 7;  // scale blocks per row
-    const uint4* src = reinterpret_cast<const uint4*>(a.src) + (size_t)t * V;
-    uint2* dst = reinterpret_cast<uint2*>(a.dst);
-    const bool lead = (threadIdx.x & 15) == 0;
+    const uint4* src = reinterpret_cast<const uint4*>(a.src) + (size_t)t * (a.H >> 3);
+    uint4* dst = reinterpret_cast<uint4*>(a.dst);
     const int lane = threadIdx.x & 31;
-    // warp-uniform trip count: every lane takes part in the half-warp shuffles
-    for (int c0 = threadIdx.x; c0 - lane < V; c0 += NT * U) {
-        uint4 v[U];
+    const bool lead = (lane & 7) == 0;
+    // warp-uniform trip count: every lane takes part in the 8-lane shuffles
+    for (int g0 = threadIdx.x; g0 - lane < G; g0 += NT * U) {
+        uint4 lo[U], hi[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int c = c0 + u * NT;
-            v[u] = (c < V) ? __ldcs(src + c) : make_uint4(0, 0, 0, 0);
+            const int g = g0 + u * NT;
+            if (g < G) {
+                lo[u] = __ldcs(src + 2 * g);
+                hi[u] = __ldcs(src + 2 * g + 1);
+            } else {
+                lo[u] = make_uint4(0, 0, 0, 0);
+                hi[u] = lo[u];
+            }
         }
-        uint2 q[U];
+        uint4 q[U];
         float sc[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            float f[8];
+            float amax = amax16(lo[u], hi[u]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                f[2 * j] = bf16_lo(w[j]);
-                f[2 * j + 1] = bf16_hi(w[j]);
-            }
-            float amax = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
-            const float scale = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-            uint32_t p[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                p[j] = e4m3x2(__fdiv_rn(f[2 * j], scale), __fdiv_rn(f[2 * j + 1], scale));
-            q[u] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
-            sc[u] = scale;
+            for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
+            sc[u] = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+            q[u] = quantize16(lo[u], hi[u], sc[u]);
         }
         for (int k = 0; k < a.K; ++k) {
             const long long row = s_dst[k];
             if (row < 0) continue;
-            uint2* d = dst + row * V;
+            uint4* d = dst + row * G;
             float* srow = a.scales + row * SB;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int c = c0 + u * NT;
-                if (c < V) {
-                    __stcs(d + c, q[u]);
-                    if (lead) __stcs(srow + (c >> 4), sc[u]);
+                const int g = g0 + u * NT;
+                if (g < G) {
+                    __stcs(d + g, q[u]);
+                    if (lead) __stcs(srow + (g >> 3), sc[u]);
                 }
             }
         }
@@ -137,7 +151,7 @@ __global__ void __launch_bounds__(NT) dispatch_fp8_kernel(MoveArgs a) {
 cudaError_t launch_dispatch(const MoveArgs& a, cudaStream_t s) {
     if (a.N == 0) return cudaSuccess;
     if (a.dtype == 0) dispatch_bf16_kernel<128, 8><<<a.N, 128, 0, s>>>(a);
-    else dispatch_fp8_kernel<128, 4><<<a.N, 128, 0, s>>>(a);
+    else dispatch_fp8_kernel<128, 2><<<a.N, 128, 0, s>>>(a);
     note_launch();
     return cudaGetLastError();
 }

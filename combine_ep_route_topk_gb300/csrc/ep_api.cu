@@ -5,7 +5,7 @@
 #include <cstdint>
 #include <cstring>
 
-#include "../../include/ep.h"
+#include "ep.h"
 #include "ep_kernels.cuh"
 
 namespace ep {

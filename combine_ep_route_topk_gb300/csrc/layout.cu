@@ -24,7 +24,7 @@
 namespace ep {
 
 int layout_chunk_tokens(int N) {
-    int C = (N + 511) / 512;  // at most ~512 chunks
+    int C = (N + 255) / 256;  // about 256 chunks at most, each a multiple of 32 tokens
     C = ((C + 31) / 32) * 32;
     return C < 32 ? 32 : C;
 }
@@ -89,6 +89,34 @@ __device__ void block_scan_inplace(int* s, int n, int* s_tmp) {
 template <int NT>
 __device__ void build_chunk_table(const int32_t* __restrict__ ro, int R, int N, int C, int* s_m,
                                   int* s_tab, int* s_tmp) {
+    if (R < 32) {  // one warp: shuffle scans over the R + 1 <= 32 entries
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            int b = 0;
+            if (lane <= R) {
+                const int v = ro[lane];
+                b = v < 0 ? 0 : (v > N ? N : v);
+            }
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(kFull, b, off);
+                if (lane >= off) b = max(b, o);
+            }
+            const int prev = __shfl_up_sync(kFull, b, 1);
+            int n = (lane >= 1 && lane <= R) ? (b - prev + C - 1) / C : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(kFull, n, off);
+                if (lane >= off) n += o;
+            }
+            if (lane <= R) {
+                s_m[lane] = b;
+                s_tab[lane] = n;
+            }
+        }
+        __syncthreads();
+        return;
+    }
     for (int r = threadIdx.x; r <= R; r += NT) {
         const int v = ro[r];
         s_m[r] = v < 0 ? 0 : (v > N ? N : v);

@@ -17,7 +17,7 @@
 // race on the array; order them on one stream.
 #include <mutex>
 
-#include "../../include/ep.h"
+#include "ep.h"
 #include "ep_kernels.cuh"
 
 namespace {

@@ -5,10 +5,11 @@
 // table's t0 row goes to experts [3, 13]); weights are a softmax over the K
 // picked logits.  One warp per token: the E logits are read once with
 // coalesced (16-byte when E is a multiple of 128) loads and held in
-// registers as order-preserving 32-bit keys; each of the K rounds is a
-// per-lane scan plus two warp reductions (redux.sync max of the key, then
-// min of the expert id among lanes holding that key, so ties go to the lower
-// id).  The winning lane clears its key.  This is HBM-bound on the N*E*4
+// registers as order-preserving 32-bit keys; each lane caches its two best
+// keys, and each of the K rounds is two warp reductions (redux.sync max of
+// the head keys, then min of the expert id among lanes holding that key, so
+// ties go to the lower id); the winning lane advances its cache and rescans
+// its registers only when both cached keys are used.  HBM-bound on the N*E*4
 // logit bytes.
 //
 // balance_map: "21K output tokens/s DeepSeek inference on AMD Instinct MI300X
@@ -39,7 +40,13 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 }
 
 // VPL logits per lane.  VEC: lane holds 4 consecutive experts of each
-// 128-wide slab (16-byte loads); else expert lane + 32 j.
+// 128-wide slab (16-byte loads); else expert lane + 32 j.  Slot j's expert id
+// increases with j, so "lower slot" means "lower id" within a lane.
+template <int VPL, bool VEC>
+__device__ __forceinline__ uint32_t expert_of(int lane, int j) {
+    return VEC ? (uint32_t)((j >> 2) * 128 + lane * 4 + (j & 3)) : (uint32_t)(lane + 32 * j);
+}
+
 template <int VPL, bool VEC>
 __global__ void __launch_bounds__(256)
 route_topk_kernel(const float* __restrict__ logits, int N, int E, int K,
@@ -50,52 +57,84 @@ route_topk_kernel(const float* __restrict__ logits, int N, int E, int K,
     if (t >= N) return;  // warp-uniform
     const float* row = logits + (size_t)t * E;
 
-    uint32_t key[VPL];
+    float v[VPL];
     if (VEC) {
 #pragma unroll
         for (int s = 0; s < VPL / 4; ++s) {
-            const float4 v = __ldcs(reinterpret_cast<const float4*>(row + s * 128 + lane * 4));
-            key[4 * s + 0] = order_key(v.x);
-            key[4 * s + 1] = order_key(v.y);
-            key[4 * s + 2] = order_key(v.z);
-            key[4 * s + 3] = order_key(v.w);
+            const float4 q = __ldcs(reinterpret_cast<const float4*>(row + s * 128 + lane * 4));
+            v[4 * s + 0] = q.x;
+            v[4 * s + 1] = q.y;
+            v[4 * s + 2] = q.z;
+            v[4 * s + 3] = q.w;
         }
     } else {
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
             const int e = lane + 32 * j;
-            key[j] = (e < E) ? order_key(__ldcs(row + e)) : 0u;
+            v[j] = (e < E) ? __ldcs(row + e) : -INFINITY;
         }
     }
-    // expert id held in slot j of this lane (increasing in j)
-    auto expert_of = [&](int j) -> uint32_t {
-        return VEC ? (uint32_t)((j >> 2) * 128 + lane * 4 + (j & 3)) : (uint32_t)(lane + 32 * j);
-    };
+    // Present slots: all but the padding past E.
+    uint32_t live = 0u;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+        if (VEC || lane + 32 * j < E) live |= 1u << j;
+
+    // This lane's two best live slots in (value desc, slot asc) order, found
+    // on the floats (-0 == +0 there); b1/b2 are their values.  A lane
+    // rescans its registers only after its second win (for 8 of 256 picks,
+    // under once per token on average); otherwise a round is two warp
+    // reductions and a few selects.
+    int s1 = -1, s2 = -1;
+    float b1 = 0.0f, b2 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+        if (!(live >> j & 1u)) continue;
+        if (s1 < 0 || v[j] > b1) {
+            s2 = s1; b2 = b1;
+            s1 = j;  b1 = v[j];
+        } else if (s2 < 0 || v[j] > b2) {
+            s2 = j;  b2 = v[j];
+        }
+    }
+    uint32_t k1 = s1 >= 0 ? order_key(b1) : 0u;
+    uint32_t k2 = s2 >= 0 ? order_key(b2) : 0u;
+    uint32_t id1 = s1 >= 0 ? expert_of<VPL, VEC>(lane, s1) : 0xffffffffu;
+    uint32_t id2 = s2 >= 0 ? expert_of<VPL, VEC>(lane, s2) : 0xffffffffu;
 
     uint32_t my_key = 0u, top_key = 0u;
     int my_id = -1;
     for (int k = 0; k < K; ++k) {
-        uint32_t bk = 0u;
-        int bj = 0;
-#pragma unroll
-        for (int j = 0; j < VPL; ++j) {
-            if (key[j] > bk) {  // strict: the lowest slot wins among equal keys
-                bk = key[j];
-                bj = j;
-            }
-        }
-        const uint32_t wmax = __reduce_max_sync(kFull, bk);
-        const uint32_t cand = (bk == wmax && bk != 0u) ? expert_of(bj) : 0xffffffffu;
+        const uint32_t wmax = __reduce_max_sync(kFull, k1);
+        const uint32_t cand = (k1 == wmax && k1 != 0u) ? id1 : 0xffffffffu;
         const uint32_t wid = __reduce_min_sync(kFull, cand);
-        if (cand == wid && cand != 0xffffffffu) {
-#pragma unroll
-            for (int j = 0; j < VPL; ++j)
-                if (j == bj) key[j] = 0u;
-        }
         if (k == 0) top_key = wmax;
         if (lane == k) {
             my_key = wmax;
             my_id = (wid == 0xffffffffu) ? -1 : (int)wid;
+        }
+        if (cand == wid && cand != 0xffffffffu) {  // this lane's head was taken
+            const int ls = s1;
+            const float lv = b1;
+            k1 = k2; id1 = id2; s1 = s2; b1 = b2;
+            k2 = 0u; id2 = 0xffffffffu; s2 = -1;
+            if (s1 < 0) {  // both cached slots used: the next two after (lv, ls)
+#pragma unroll
+                for (int j = 0; j < VPL; ++j) {
+                    const bool after = (live >> j & 1u) && (v[j] < lv || (v[j] == lv && j > ls));
+                    if (!after) continue;
+                    if (s1 < 0 || v[j] > b1) {
+                        s2 = s1; b2 = b1;
+                        s1 = j;  b1 = v[j];
+                    } else if (s2 < 0 || v[j] > b2) {
+                        s2 = j;  b2 = v[j];
+                    }
+                }
+                k1 = s1 >= 0 ? order_key(b1) : 0u;
+                k2 = s2 >= 0 ? order_key(b2) : 0u;
+                id1 = s1 >= 0 ? expert_of<VPL, VEC>(lane, s1) : 0xffffffffu;
+                id2 = s2 >= 0 ? expert_of<VPL, VEC>(lane, s2) : 0xffffffffu;
+            }
         }
     }
 
