@@ -210,13 +210,24 @@ def run_ours(args, world, rank, local):
     comb = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
+    fused = args.fused
+    ws_fused = torch.empty(ep.ep_route_layout_workspace_size(N, E, K, R), dtype=torch.uint8,
+                           device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        ep.ep_route_topk(logits, K, topk_idx=idx, topk_w=wt)
-        if ev:
-            ev[1].record(stream)
-        ep.ep_dispatch_layout(idx, ro, E, 0, out=lay, workspace=ws)
+        if fused:  # route + layout in one cooperative kernel
+            ep.ep_route_layout(logits, ro, K, 0, topk_idx=idx, topk_w=wt, out=lay,
+                               status=status, workspace=ws_fused)
+            if ev:
+                ev[1].record(stream)
+        else:
+            ep.ep_route_topk(logits, K, topk_idx=idx, topk_w=wt)
+            if ev:
+                ev[1].record(stream)
+            ep.ep_dispatch_layout(idx, ro, E, 0, out=lay, workspace=ws)
         if ev:
             ev[2].record(stream)
         ep.ep_dispatch(x, idx, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_CONTIG, 0,
@@ -247,8 +258,11 @@ def run_ours(args, world, rank, local):
     barrier(dist)
     launches = ep.ep_kernel_launch_count() - launches0
     clocks = sampler.stop() if sampler else None
+    if int(status.item()) != 0:
+        raise RuntimeError("route+layout kernel reported a barrier timeout")
 
     overlap = two_batch_overlap(args, ep, torch, dev, stream, inp, w, flush, dist)
+    decode = decode_latency(args, ep, torch, dev, stream, flush) if rank == 0 else None
 
     stage = {n: [e[j].elapsed_time(e[j + 1]) for e in evs]
              for j, n in enumerate(["route", "layout", "dispatch", "combine"])}
@@ -297,7 +311,10 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = measured_peaks()
     mean = {k: statistics.fmean(v) for k, v in stage.items()}
     kernels = {}
-    for k in ["route", "layout", "dispatch", "combine"]:
+    if fused:  # one kernel for route + layout: report it as one stage
+        mean["route_layout"] = mean.pop("route") + mean.pop("layout")
+        bm["route_layout"] = bm["route"] + bm["layout"]
+    for k in (["route_layout"] if fused else ["route", "layout"]) + ["dispatch", "combine"]:
         gbs = bm[k] / (mean[k] / 1e3) / 1e9
         kernels[k] = {"ms": round(mean[k], 4), "bytes": bm[k], "GB/s": round(gbs, 1),
                       "frac_of_measured": round(gbs / peak, 4),
@@ -326,7 +343,8 @@ def run_ours(args, world, rank, local):
                    f"prefill shape at 8 ranks x {args.tokens_per_rank} tokens",
                    "R": w.R, "N": N, "E": E, "K": K, "H": H,
                    "layout": "contiguous", "dispatch_dtype": "fp8_e4m3_1x128",
-                   "step": "route+layout+dispatch+combine",
+                   "step": ("route+layout (one fused kernel)" if fused else
+                            "route, layout") + ", dispatch, combine",
                    "l2": "flushed between steps (512 MiB write, outside the step events); "
                          "inputs (x 0.47 GB, y 3.76 GB) also exceed L2",
                    "parallelism": f"{world} independent replica(s), one per GPU"},
@@ -342,6 +360,7 @@ def run_ours(args, world, rank, local):
                                                    4)},
         "kernels": kernels,
         "two_batch_overlap": overlap,
+        "decode_step": decode,
         "e2e": {"value": round(tok * e2e_steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms / e2e_steps, 3), "steps": e2e_steps},
@@ -422,6 +441,72 @@ def two_batch_overlap(args, ep, torch, dev, main_stream, inp, w, flush, dist):
     return {"tokens_per_s": round(tok * steps / (total / 1e3), 1),
             "ms_per_step": round(total / steps, 4), "steps": steps,
             "note": "ranks 0..3 and 4..7 as two micro-batches on two streams"}
+
+
+def decode_latency(args, ep, torch, dev, stream, flush):
+    """Latency of one decode step (the low-latency, masked layout): 8 ranks x
+    128 tokens, E=256, K=8, H=7168, capacity 128; route + layout (fused
+    kernel, and as separate kernels), masked bf16 dispatch, masked combine.
+    L2 flushed before every step."""
+    from combine_ep_route_topk_gb300 import workloads as wl
+    w = wl.WORKLOADS["decode"]
+    inp = wl.make_inputs(w, seed=args.seed + 1, device=str(dev))
+    N, E, K, H, R, cap = inp["N"], w.E, w.K, w.H, w.R, w.cap
+    idx = torch.empty(N, K, dtype=torch.int32, device=dev)
+    wt = torch.empty(N, K, dtype=torch.float32, device=dev)
+    lay = ep.alloc_layout(N, E, K, R, cap, dev)
+    ws = torch.empty(max(ep.ep_route_layout_workspace_size(N, E, K, R),
+                         ep.ep_dispatch_layout_workspace_size(N, E, K, R)), dtype=torch.uint8,
+                     device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty(E * cap, H, dtype=torch.bfloat16, device=dev)
+    comb = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+
+    def step(fused):
+        if fused:
+            ep.ep_route_layout(inp["logits"], inp["rank_offsets"], K, cap, topk_idx=idx,
+                               topk_w=wt, out=lay, status=st, workspace=ws)
+        else:
+            ep.ep_route_topk(inp["logits"], K, topk_idx=idx, topk_w=wt)
+            ep.ep_dispatch_layout(idx, inp["rank_offsets"], E, cap, out=lay, workspace=ws)
+        ep.ep_dispatch(inp["x"], idx, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_MASKED, cap,
+                       out=out)
+        ep.ep_combine(inp["y"], idx, wt, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_MASKED,
+                      cap, out=comb)
+
+    res = {}
+    for fused in (True, False):
+        for i in range(3):
+            step(fused)
+        torch.cuda.synchronize()
+        # the step captured once in a CUDA graph (the low-latency mode's
+        # static shapes allow it), so the timing is the GPU's, not Python's
+        # launch path; eager launches are timed too for comparison
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step(fused)
+        for mode in ("graph", "eager"):
+            n = 100
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+            for i in range(n):
+                flush.fill_(i & 0xFF)
+                evs[i][0].record(stream)
+                if mode == "graph":
+                    graph.replay()
+                else:
+                    step(fused)
+                evs[i][1].record(stream)
+            torch.cuda.synchronize()
+            ts = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+            key = ("fused" if fused else "separate") + "_route_layout_" + mode
+            res[key] = {"us_median": round(ts[n // 2], 2), "us_min": round(ts[0], 2),
+                        "tokens_per_s": round(N / (ts[n // 2] / 1e6), 1)}
+        del graph
+    if int(st.item()) != 0:
+        raise RuntimeError("route+layout kernel reported a barrier timeout")
+    res["workload"] = "decode: 8 ranks x 128 tokens, E=256, K=8, H=7168, masked cap 128, bf16"
+    return res
 
 
 # ------------------------------------------------------------- CPU oracle --
@@ -508,6 +593,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--fused", action="store_true",
+                    help="route + layout as the one cooperative kernel (ep_route_layout)")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="run a smaller case of the workload (default: the full 4096)")
     args = ap.parse_args(argv)

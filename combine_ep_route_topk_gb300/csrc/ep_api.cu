@@ -125,6 +125,73 @@ ep_status_t ep_dispatch_layout(const int32_t* topk_idx, const int32_t* rank_offs
     return cuda_status(launch_layout(a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t ep_route_layout_workspace_size(int32_t N, int32_t E, int32_t K, int32_t R) {
+    if (N < 0) N = 0;
+    if (E < 1) E = 1;
+    if (R < 1) R = 1;
+    return route_layout_workspace_bytes(N, E, K, R);
+}
+
+ep_status_t ep_route_layout(const float* logits, const int32_t* rank_offsets, int32_t R,
+                            int32_t N, int32_t E, int32_t K, const int32_t* expert_map,
+                            int32_t cap, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                            int32_t* expert_offsets, int32_t* rank_expert_offsets, int32_t* pos,
+                            int32_t* row_src, int32_t* masked_m, int32_t* overflow_count,
+                            int32_t* status, void* workspace, size_t ws_bytes, void* stream) {
+    ep_status_t st = check_sizes(N, E, K);
+    if (st != EP_OK) return st;
+    if (R < 1) return EP_ERR_INVALID_ARG;
+    if (R > kMaxR) return EP_ERR_UNSUPPORTED;
+    if (cap < 0) return EP_ERR_INVALID_ARG;
+    if ((masked_m || overflow_count) && cap == 0) return EP_ERR_INVALID_ARG;
+    if (!rank_offsets || !counts || !expert_offsets || !rank_expert_offsets)
+        return EP_ERR_INVALID_ARG;
+    if (N > 0 && (!logits || !topk_idx || !topk_w || !pos || !row_src)) return EP_ERR_INVALID_ARG;
+    const void* ptrs[] = {logits, rank_offsets, expert_map, topk_idx, topk_w, counts,
+                          expert_offsets, rank_expert_offsets, pos, row_src, masked_m,
+                          overflow_count, status};
+    for (const void* p : ptrs)
+        if (!aligned4(p)) return EP_ERR_INVALID_ARG;
+    const size_t need = route_layout_workspace_bytes(N, E, K, R);
+    if (!workspace || ws_bytes < need || !aligned16(workspace)) return EP_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    LayoutArgs a;
+    a.topk_idx = topk_idx;
+    a.rank_offsets = rank_offsets;
+    a.R = R;
+    a.N = N;
+    a.E = E;
+    a.K = K;
+    a.cap = cap;
+    a.counts = counts;
+    a.expert_offsets = expert_offsets;
+    a.rank_expert_offsets = rank_expert_offsets;
+    a.pos = pos;
+    a.row_src = row_src;
+    a.masked_m = masked_m;
+    a.overflow = overflow_count;
+    a.ws_hist = nullptr;
+    a.ws_totals = nullptr;
+    RouteLayoutArgs r;
+    r.lay = a;
+    r.logits = logits;
+    r.emap = expert_map;
+    r.topk_idx = topk_idx;
+    r.topk_w = topk_w;
+    r.status = status;
+    r.workspace = static_cast<int32_t*>(workspace);
+    bool launched = false;
+    cudaError_t err = launch_route_layout(r, s, &launched);
+    if (err != cudaSuccess) return cuda_status(err);
+    if (launched) return EP_OK;
+    // no fused instance for these sizes: the same results from the two kernels
+    err = launch_route_topk(logits, N, E, K, expert_map, topk_idx, topk_w, s);
+    if (err != cudaSuccess) return cuda_status(err);
+    a.ws_hist = static_cast<int32_t*>(workspace);
+    a.ws_totals = a.ws_hist + (size_t)layout_chunk_slots(N, R) * E;
+    return cuda_status(launch_layout(a, s));
+}
+
 static ep_status_t check_move(const void* src, int32_t N, int32_t H, int32_t E, int32_t K,
                               const int32_t* topk_idx, const int32_t* pos,
                               const int32_t* expert_offsets, ep_layout_t layout, int32_t cap,

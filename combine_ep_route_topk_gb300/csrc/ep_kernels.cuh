@@ -49,6 +49,25 @@ struct LayoutArgs {
 };
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t s);
 
+// ---- fused route + layout (one cooperative kernel) ------------------------
+int route_layout_chunk_tokens(int N);
+int route_layout_chunk_slots(int N, int R);
+// Workspace for the fused kernel and for the two-step fallback.
+size_t route_layout_workspace_bytes(int N, int E, int K, int R);
+
+struct RouteLayoutArgs {
+    LayoutArgs lay;          // lay.topk_idx aliases topk_idx; lay.ws_* unused
+    const float* logits;
+    const int32_t* emap;
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* status;         // device int32 or nullptr
+    int32_t* workspace;
+};
+// *launched is false when the sizes have no fused instance or the device
+// cannot hold a block of it; the caller then runs route and layout kernels.
+cudaError_t launch_route_layout(const RouteLayoutArgs& r, cudaStream_t s, bool* launched);
+
 // ---- dispatch / combine --------------------------------------------------
 struct MoveArgs {
     const void* src;            // x (dispatch) or y (combine)

@@ -1,0 +1,238 @@
+// Fused route + layout for sm_103a: one cooperative, persistent kernel that
+// computes exactly what ep_route_topk followed by ep_dispatch_layout compute
+// ("Anatomy of a High-Performance EP Kernel": route locally, then "ask first,
+// then send"), without the launches and ramp-ups in between.
+//
+//   phase 1  each block takes chunks of C tokens (chunks never straddle a
+//            rank); each warp routes tokens of the chunk (route::route_token)
+//            and the block counts the chunk's picks per expert in shared
+//            memory, then writes the chunk histogram row.
+//   barrier
+//   phase 2  one block per expert column scans the chunk histograms down the
+//            chunks (exclusive prefixes, expert total, per-rank counts and
+//            offsets).
+//   barrier
+//   phase 3  expert offsets from the totals, side outputs, and the stable
+//            per-chunk scatter of positions (lay::scatter_chunk).
+//
+// The grid never exceeds the blocks that can be resident at once (the launch
+// is cooperative), so every block reaches each barrier.  A barrier is a
+// counter in the workspace, zeroed by a memset before the launch; each wait
+// is bounded (kSpinLimit polls with a back-off) and, if it ever ran out, the
+// block would record 1 in `status` and return instead of waiting on.
+#include "ep.h"
+#include "ep_kernels.cuh"
+#include "layout_common.cuh"
+#include "route_common.cuh"
+
+namespace ep {
+
+int route_layout_chunk_tokens(int N) {
+    int C = (N + 1023) / 1024;  // up to ~1024 chunks: routing wants many warps
+    C = ((C + 31) / 32) * 32;
+    return C < 32 ? 32 : C;
+}
+
+int route_layout_chunk_slots(int N, int R) {
+    const int C = route_layout_chunk_tokens(N);
+    return (N + C - 1) / C + R;
+}
+
+size_t route_layout_workspace_bytes(int N, int E, int K, int R) {
+    const size_t slots = (size_t)route_layout_chunk_slots(N, R);
+    size_t b = (slots * (size_t)E + (size_t)E + 64) * sizeof(int32_t);
+    b = ((b + 255) / 256) * 256;
+    const size_t sep = layout_workspace_bytes(N, E, K, R);  // fallback path
+    return b > sep ? b : sep;
+}
+
+namespace {
+
+using namespace lay;
+
+constexpr unsigned kSpinLimit = 1u << 22;
+
+struct FusedArgs {
+    LayoutArgs a;            // a.topk_idx aliases topk_idx below
+    const float* logits;
+    const int32_t* emap;
+    int32_t* topk_idx;
+    float* topk_w;
+    unsigned* bar;           // two barrier counters, zero at launch
+    int32_t* status;         // may be null
+};
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid-wide barrier over a co-resident grid.  Returns false (after recording
+// the failure) if the wait ran out, which a cooperative launch rules out.
+__device__ bool grid_barrier(unsigned* ctr, int32_t* status) {
+    __syncthreads();
+    int ok = 1;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(ctr, 1u);
+        unsigned polls = 0;
+        while (ld_acquire_gpu(ctr) < gridDim.x) {
+            if (++polls > kSpinLimit) {
+                ok = 0;
+                if (status) atomicExch(status, 1);
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();
+    }
+    return __syncthreads_and(ok) != 0;
+}
+
+template <int VPL, bool VEC, int KT>
+__global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
+    extern __shared__ int smem[];
+    const LayoutArgs& a = f.a;
+    int* s_m = smem;
+    int* s_tab = s_m + round_up4(a.R + 1);
+    int* s_tmp = s_tab + round_up4(a.R + 1);
+    int* s_eoff = s_tmp + 32;                // [E+1]
+    int* s_w = s_eoff + round_up4(a.E + 1);   // [warps][E]; phase 1: one histogram
+    build_chunk_table<kNT>(a.rank_offsets, a.R, a.N, C, s_m, s_tab, s_tmp);
+    const int S = s_tab[a.R];
+    const int E = a.E;
+    const int K = KT > 0 ? KT : a.K;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+    // ---- phase 1: route the chunk's tokens, count its picks per expert
+    for (int c = blockIdx.x; c < S; c += gridDim.x) {
+        for (int e = threadIdx.x; e < E; e += kNT) s_w[e] = 0;
+        __syncthreads();
+        const int r = chunk_rank(s_tab, a.R, c);
+        const int tok0 = s_m[r] + (c - s_tab[r]) * C;
+        const int tok1 = min(tok0 + C, s_m[r + 1]);
+        for (int t = tok0 + warp; t < tok1; t += kWarps) {
+            int id;
+            float w;
+            route::route_token<VPL, VEC, KT>(f.logits + (size_t)t * E, E, a.K, f.emap, lane, id,
+                                             w);
+            if (lane < K) {
+                f.topk_idx[(size_t)t * K + lane] = id;
+                f.topk_w[(size_t)t * K + lane] = w;
+                if (id >= 0) atomicAdd(&s_w[id], 1);
+            }
+        }
+        __syncthreads();
+        int* row = a.ws_hist + (size_t)c * E;
+        for (int e = threadIdx.x; e < E; e += kNT) row[e] = s_w[e];
+        __syncthreads();
+    }
+    if (!grid_barrier(f.bar + 0, f.status)) return;
+
+    // ---- phase 2: one block per expert column
+    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+        int* hist = a.ws_hist;
+        const int per = (S + kNT - 1) / kNT;
+        const int r0 = min(S, (int)threadIdx.x * per), r1 = min(S, r0 + per);
+        int sum = 0;
+        for (int c = r0; c < r1; ++c) sum += __ldcg(hist + (size_t)c * E + e);
+        s_w[threadIdx.x] = sum;
+        __syncthreads();
+        block_scan_inplace<kNT, false>(s_w, kNT, s_tmp);
+        int run = s_w[threadIdx.x] - sum;
+        const int total = s_w[kNT - 1];
+        for (int c = r0; c < r1; ++c) {
+            const size_t at = (size_t)c * E + e;
+            const int v = __ldcg(hist + at);
+            hist[at] = run;
+            run += v;
+        }
+        if (threadIdx.x == 0) a.ws_totals[e] = total;
+        __syncthreads();
+        for (int r = threadIdx.x; r < a.R; r += kNT) {
+            const int lo = s_tab[r], hi = s_tab[r + 1];
+            const int pre_lo = (lo < S) ? __ldcg(hist + (size_t)lo * E + e) : total;
+            const int pre_hi = (hi < S) ? __ldcg(hist + (size_t)hi * E + e) : total;
+            a.counts[(size_t)r * E + e] = pre_hi - pre_lo;
+            a.rank_expert_offsets[(size_t)r * E + e] = pre_lo;
+        }
+        __syncthreads();
+    }
+    if (!grid_barrier(f.bar + 1, f.status)) return;
+
+    // ---- phase 3: offsets, side outputs, stable positions
+    load_expert_offsets<kNT>(a.ws_totals, E, s_eoff, s_tmp);
+    side_outputs<kNT>(a, s_eoff, s_tmp, blockIdx.x, gridDim.x);
+    for (int c = blockIdx.x; c < S; c += gridDim.x)
+        scatter_chunk<kNT>(a, c, C, s_m, s_tab, s_eoff, s_w);
+}
+
+template <int VPL, bool VEC, int KT>
+cudaError_t launch_fused_t(FusedArgs& f, int C, int slots, size_t smem, cudaStream_t s,
+                           bool* launched) {
+    auto* fn = route_layout_kernel<VPL, VEC, KT>;
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kNT, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaSuccess;  // not launched: caller falls back
+    int grid = per_sm * sm_count();
+    if (grid > slots) grid = slots;
+    if (grid < 1) grid = 1;
+    void* args[] = {&f, &C};
+    err = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kNT),
+                                      args, smem, s);
+    if (err == cudaSuccess) {
+        *launched = true;
+        note_launch();
+    }
+    return err;
+}
+
+}  // namespace
+
+cudaError_t launch_route_layout(const RouteLayoutArgs& r, cudaStream_t s, bool* launched) {
+    *launched = false;
+    const LayoutArgs& a = r.lay;
+    const int C = route_layout_chunk_tokens(a.N);
+    const int slots = route_layout_chunk_slots(a.N, a.R);
+    FusedArgs f;
+    f.a = a;
+    f.a.ws_hist = r.workspace;
+    f.a.ws_totals = r.workspace + (size_t)slots * a.E;
+    f.logits = r.logits;
+    f.emap = r.emap;
+    f.topk_idx = r.topk_idx;
+    f.topk_w = r.topk_w;
+    f.bar = reinterpret_cast<unsigned*>(f.a.ws_totals + a.E);
+    f.status = r.status;
+    const bool vec = (a.E % 128 == 0) && ((reinterpret_cast<uintptr_t>(r.logits) & 15u) == 0);
+    const size_t smem = (size_t)(2 * ((a.R + 1 + 3) & ~3) + 32 + ((a.E + 1 + 3) & ~3) +
+                                 kWarps * (a.E > kNT ? a.E : kNT)) * sizeof(int);
+    cudaError_t err = cudaMemsetAsync(f.bar, 0, 2 * sizeof(unsigned), s);
+    if (err == cudaSuccess && r.status) err = cudaMemsetAsync(r.status, 0, sizeof(int32_t), s);
+    if (err != cudaSuccess) return err;
+    const int K = a.K;
+    if (vec && a.E == 256) {
+        if (K == 8) return launch_fused_t<8, true, 8>(f, C, slots, smem, s, launched);
+        if (K == 4) return launch_fused_t<8, true, 4>(f, C, slots, smem, s, launched);
+        return launch_fused_t<8, true, 0>(f, C, slots, smem, s, launched);
+    }
+    if (vec && a.E == 128) {
+        if (K == 8) return launch_fused_t<4, true, 8>(f, C, slots, smem, s, launched);
+        if (K == 4) return launch_fused_t<4, true, 4>(f, C, slots, smem, s, launched);
+        return launch_fused_t<4, true, 0>(f, C, slots, smem, s, launched);
+    }
+    if (vec && a.E == 512) return launch_fused_t<16, true, 0>(f, C, slots, smem, s, launched);
+    if (vec && a.E == 1024) return launch_fused_t<32, true, 0>(f, C, slots, smem, s, launched);
+    if (a.E <= 32) {
+        if (K == 2) return launch_fused_t<1, false, 2>(f, C, slots, smem, s, launched);
+        return launch_fused_t<1, false, 0>(f, C, slots, smem, s, launched);
+    }
+    if (a.E <= 64) return launch_fused_t<2, false, 0>(f, C, slots, smem, s, launched);
+    if (a.E <= 128) return launch_fused_t<4, false, 0>(f, C, slots, smem, s, launched);
+    if (a.E <= 256) return launch_fused_t<8, false, 0>(f, C, slots, smem, s, launched);
+    return cudaSuccess;  // other sizes: not launched, the caller runs the two-step path
+}
+
+}  // namespace ep

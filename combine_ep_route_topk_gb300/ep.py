@@ -45,6 +45,11 @@ def lib():
         L.ep_dispatch_layout_workspace_size.restype = sz
         L.ep_dispatch_layout.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P,
                                          sz, P]
+        L.ep_route_layout_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.ep_route_layout_workspace_size.restype = sz
+        L.ep_route_layout.argtypes = [P, P, i32, i32, i32, i32, P, i32, P, P, P, P, P, P, P, P, P,
+                                      P, P, sz, P]
+        L.ep_route_layout.restype = ctypes.c_int
         L.ep_dispatch.argtypes = [P, i32, i32, i32, i32, P, P, P, ctypes.c_int, i32, ctypes.c_int,
                                   P, P, P]
         L.ep_combine.argtypes = [P, i32, i32, i32, i32, P, P, P, P, ctypes.c_int, i32, P, P]
@@ -162,6 +167,43 @@ def ep_dispatch_layout(topk_idx, rank_offsets, E, cap=0, out: Layout | None = No
         _opt(out.overflow_count, torch.int32, "overflow_count", (1,)),
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
     return out
+
+
+def ep_route_layout_workspace_size(N, E, K, R) -> int:
+    return int(lib().ep_route_layout_workspace_size(N, E, K, R))
+
+
+def ep_route_layout(logits, rank_offsets, K, cap=0, expert_map=None, topk_idx=None,
+                    topk_w=None, out: Layout | None = None, status=None, workspace=None,
+                    stream=None):
+    """ep_route_topk + ep_dispatch_layout in one cooperative kernel.
+    Returns (topk_idx, topk_w, Layout)."""
+    N, E = logits.shape
+    R = rank_offsets.shape[0] - 1
+    if topk_idx is None:
+        topk_idx = _empty((N, K), torch.int32, logits)
+    if topk_w is None:
+        topk_w = _empty((N, K), torch.float32, logits)
+    if out is None:
+        out = alloc_layout(N, E, K, R, cap, logits.device)
+    need = ep_route_layout_workspace_size(N, E, K, R)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=logits.device)
+    _check("ep_route_layout", lib().ep_route_layout(
+        _dev(logits, torch.float32, "logits"), _dev(rank_offsets, torch.int32, "rank_offsets"),
+        R, N, E, K, _opt(expert_map, torch.int32, "expert_map", (E,)), cap,
+        _dev(topk_idx, torch.int32, "topk_idx", (N, K)),
+        _dev(topk_w, torch.float32, "topk_w", (N, K)),
+        _dev(out.counts, torch.int32, "counts", (R, E)),
+        _dev(out.expert_offsets, torch.int32, "expert_offsets", (E + 1,)),
+        _dev(out.rank_expert_offsets, torch.int32, "rank_expert_offsets", (R, E)),
+        _dev(out.pos, torch.int32, "pos", (N, K)),
+        _dev(out.row_src, torch.int32, "row_src", (N * K,)),
+        _opt(out.masked_m, torch.int32, "masked_m", (E,)),
+        _opt(out.overflow_count, torch.int32, "overflow_count", (1,)),
+        _opt(status, torch.int32, "status", (1,)),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+    return topk_idx, topk_w, out
 
 
 def dispatch_rows(N, K, E, layout, cap):

@@ -36,7 +36,8 @@
  *   - Arguments are checked on the host before anything is launched; a bad
  *     argument returns EP_ERR_INVALID_ARG (or EP_ERR_WORKSPACE /
  *     EP_ERR_UNSUPPORTED) and launches nothing.  A failed launch returns
- *     EP_ERR_CUDA.  No kernel traps, asserts or waits on another kernel.
+ *     EP_ERR_CUDA.  No kernel traps, asserts or waits on another kernel; the
+ *     only waits are the bounded grid barriers inside ep_route_layout.
  *   - Device-side data that break a precondition (an expert id outside
  *     [0,E), rank_offsets that are not a non-decreasing 0..N sequence, pos
  *     values that do not come from ep_dispatch_layout) never cause an access
@@ -148,6 +149,30 @@ ep_status_t ep_dispatch_layout(const int32_t* topk_idx, const int32_t* rank_offs
                                int32_t* rank_expert_offsets, int32_t* pos, int32_t* row_src,
                                int32_t* masked_m, int32_t* overflow_count,
                                void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace ep_route_layout needs (a multiple of 256). */
+size_t ep_route_layout_workspace_size(int32_t N, int32_t E, int32_t K, int32_t R);
+
+/*
+ * ep_route_layout -- ep_route_topk followed by ep_dispatch_layout in one
+ * cooperative persistent kernel (no launches or ramp-ups in between); same
+ * arguments and bit-identical outputs as the two calls.  [Anatomy] "What we
+ * have to do" (route locally) and "High throughput: ask first, then send".
+ *   status    int32 [1] device, or NULL: 0 when the call completed, 1 if a
+ *             block's bounded wait at an internal grid barrier ran out
+ *             (results then incomplete; the co-resident launch rules it out).
+ *   workspace ep_route_layout_workspace_size bytes, no initialisation needed.
+ * Sizes without a fused instance (E not a multiple of 128 above 256 experts)
+ * or a device that cannot hold one block run the two kernels instead, with
+ * the same results.  Launches two small memsets (barrier counters, status)
+ * before the kernel.
+ */
+ep_status_t ep_route_layout(const float* logits, const int32_t* rank_offsets, int32_t R,
+                            int32_t N, int32_t E, int32_t K, const int32_t* expert_map,
+                            int32_t cap, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                            int32_t* expert_offsets, int32_t* rank_expert_offsets, int32_t* pos,
+                            int32_t* row_src, int32_t* masked_m, int32_t* overflow_count,
+                            int32_t* status, void* workspace, size_t ws_bytes, void* stream);
 
 /* Bytes of the fixed scratch array that ep_dispatch_layout_static keeps
  * inside the library on every GPU that loads it (4 MiB). */
