@@ -595,13 +595,24 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--fused", action="store_true",
                     help="route + layout as the one cooperative kernel (ep_route_layout)")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the decode step (for profiling its kernels)")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="run a smaller case of the workload (default: the full 4096)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
-    if args.impl == "reference":
+    if args.decode_only:
+        import torch
+        import combine_ep_route_topk_gb300 as ep
+        torch.cuda.set_device(local)
+        dev = torch.device("cuda", local)
+        stream = torch.cuda.Stream(device=dev)
+        torch.cuda.set_stream(stream)
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        line = {"decode_step": decode_latency(args, ep, torch, dev, stream, flush)}
+    elif args.impl == "reference":
         line = run_reference(args, world, rank)
     else:
         line = run_ours(args, world, rank, local)

@@ -22,9 +22,9 @@
 namespace ep {
 
 int layout_chunk_tokens(int N) {
-    int C = (N + 255) / 256;  // about 256 chunks at most, each a multiple of 32 tokens
-    C = ((C + 31) / 32) * 32;
-    return C < 32 ? 32 : C;
+    int C = (N + 255) / 256;  // about 256 chunks at most, each a multiple of 8 tokens
+    C = ((C + 7) / 8) * 8;
+    return C < 8 ? 8 : C;
 }
 
 int layout_chunk_slots(int N, int R) {

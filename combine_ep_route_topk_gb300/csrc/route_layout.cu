@@ -8,9 +8,10 @@
 //            and the block counts the chunk's picks per expert in shared
 //            memory, then writes the chunk histogram row.
 //   barrier
-//   phase 2  one block per expert column scans the chunk histograms down the
-//            chunks (exclusive prefixes, expert total, per-rank counts and
-//            offsets).
+//   phase 2  blocks take tiles of 32 expert columns; each warp scans a group
+//            of chunk rows (coalesced 128-byte reads) and the block combines
+//            the groups: exclusive prefixes, expert totals, per-rank counts
+//            and offsets.
 //   barrier
 //   phase 3  expert offsets from the totals, side outputs, and the stable
 //            per-chunk scatter of positions (lay::scatter_chunk).
@@ -29,8 +30,8 @@ namespace ep {
 
 int route_layout_chunk_tokens(int N) {
     int C = (N + 1023) / 1024;  // up to ~1024 chunks: routing wants many warps
-    C = ((C + 31) / 32) * 32;
-    return C < 32 ? 32 : C;
+    C = ((C + 7) / 8) * 8;      // 8 tokens = one per warp of a block
+    return C < 8 ? 8 : C;
 }
 
 int route_layout_chunk_slots(int N, int R) {
@@ -130,32 +131,47 @@ __global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
     }
     if (!grid_barrier(f.bar + 0, f.status)) return;
 
-    // ---- phase 2: one block per expert column
-    for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    // ---- phase 2: tiles of 32 expert columns; warp w scans row group w, so
+    // every row read is one coalesced 128-byte line per warp
+    for (int tile = blockIdx.x; tile * 32 < E; tile += gridDim.x) {
         int* hist = a.ws_hist;
-        const int per = (S + kNT - 1) / kNT;
-        const int r0 = min(S, (int)threadIdx.x * per), r1 = min(S, r0 + per);
+        const int e = tile * 32 + lane;
+        const bool live = e < E;
+        const int rpg = (S + kWarps - 1) / kWarps;
+        const int r0 = min(S, warp * rpg), r1 = min(S, r0 + rpg);
         int sum = 0;
-        for (int c = r0; c < r1; ++c) sum += __ldcg(hist + (size_t)c * E + e);
-        s_w[threadIdx.x] = sum;
+        if (live)
+            for (int c = r0; c < r1; ++c) sum += __ldcg(hist + (size_t)c * E + e);
+        s_w[warp * 32 + lane] = sum;
         __syncthreads();
-        block_scan_inplace<kNT, false>(s_w, kNT, s_tmp);
-        int run = s_w[threadIdx.x] - sum;
-        const int total = s_w[kNT - 1];
-        for (int c = r0; c < r1; ++c) {
-            const size_t at = (size_t)c * E + e;
-            const int v = __ldcg(hist + at);
-            hist[at] = run;
-            run += v;
+        int run = 0, total = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            const int v = s_w[w * 32 + lane];
+            if (w < warp) run += v;
+            total += v;
         }
-        if (threadIdx.x == 0) a.ws_totals[e] = total;
+        if (live)
+            for (int c = r0; c < r1; ++c) {
+                const size_t at = (size_t)c * E + e;
+                const int v = __ldcg(hist + at);
+                hist[at] = run;
+                run += v;
+            }
+        if (warp == 0) {
+            s_w[kWarps * 32 + lane] = total;
+            if (live) a.ws_totals[e] = total;
+        }
         __syncthreads();
-        for (int r = threadIdx.x; r < a.R; r += kNT) {
+        for (int idx = threadIdx.x; idx < a.R * 32; idx += kNT) {
+            const int r = idx >> 5, cc = idx & 31;
+            const int ee = tile * 32 + cc;
+            if (ee >= E) continue;
+            const int tot = s_w[kWarps * 32 + cc];
             const int lo = s_tab[r], hi = s_tab[r + 1];
-            const int pre_lo = (lo < S) ? __ldcg(hist + (size_t)lo * E + e) : total;
-            const int pre_hi = (hi < S) ? __ldcg(hist + (size_t)hi * E + e) : total;
-            a.counts[(size_t)r * E + e] = pre_hi - pre_lo;
-            a.rank_expert_offsets[(size_t)r * E + e] = pre_lo;
+            const int pre_lo = (lo < S) ? __ldcg(hist + (size_t)lo * E + ee) : tot;
+            const int pre_hi = (hi < S) ? __ldcg(hist + (size_t)hi * E + ee) : tot;
+            a.counts[(size_t)r * E + ee] = pre_hi - pre_lo;
+            a.rank_expert_offsets[(size_t)r * E + ee] = pre_lo;
         }
         __syncthreads();
     }
