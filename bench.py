@@ -262,6 +262,8 @@ def run_ours(args, world, rank, local):
         raise RuntimeError("route+layout kernel reported a barrier timeout")
 
     overlap = two_batch_overlap(args, ep, torch, dev, stream, inp, w, flush, dist)
+    chunk = chunked_prefill(args, ep, torch, dev, stream, inp, w, flush, dist,
+                            T=min(8192, max(8, inp["N"] // 4)))
     decode = decode_latency(args, ep, torch, dev, stream, flush) if rank == 0 else None
 
     stage = {n: [e[j].elapsed_time(e[j + 1]) for e in evs]
@@ -360,6 +362,7 @@ def run_ours(args, world, rank, local):
                                                    4)},
         "kernels": kernels,
         "two_batch_overlap": overlap,
+        "chunked_rounds": chunk,
         "decode_step": decode,
         "e2e": {"value": round(tok * e2e_steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -376,54 +379,48 @@ def run_ours(args, world, rank, local):
 
 
 def two_batch_overlap(args, ep, torch, dev, main_stream, inp, w, flush, dist):
-    """The same batch as two micro-batches (ranks 0..R/2-1 and R/2..R-1), each
-    running route -> layout -> dispatch -> combine on its own stream, so that
-    one micro-batch's latency-bound routing and layout overlap the other's
-    HBM-bound dispatch and combine (the two-batch overlap of the pages'
-    serving systems, on one GPU).  Same per-token work; each micro-batch has
-    its own expert-major layout."""
-    E, K, H, R = w.E, w.K, w.H, w.R
+    """The same batch as two micro-batches (ranks 0..R/2-1 and R/2..R-1) on two
+    streams (pipeline.two_batch_overlap): one micro-batch's latency-bound
+    routing and layout overlap the other's HBM-bound dispatch and combine."""
+    from combine_ep_route_topk_gb300 import pipeline as pl
+    K, H = w.K, w.H
+    comb = torch.empty(inp["N"], H, dtype=torch.bfloat16, device=dev)
+    mbs = pl.make_micro_batches(inp["logits"], inp["x"], inp["rank_offsets"], K,
+                                ep.EP_DTYPE_FP8_E4M3_B128, comb)
+    y = inp["y"]
+
+    def step():
+        pl.two_batch_overlap(mbs, K, ep.EP_DTYPE_FP8_E4M3_B128,
+                             lambda mb: y[mb.t0 * K:mb.t1 * K], main_stream)
+
+    return _time_schedule(args, torch, main_stream, flush, dist, step, inp["N"],
+                          "ranks 0..3 and 4..7 as two micro-batches on two streams")
+
+
+def chunked_prefill(args, ep, torch, dev, main_stream, inp, w, flush, dist, T=8192):
+    """The same batch in ant-moving rounds of T tokens (pipeline.chunked): the
+    dispatch buffer holds T*K rows instead of N*K."""
+    from combine_ep_route_topk_gb300 import pipeline as pl
+    K, H, E, R = w.K, w.H, w.E, w.R
+    comb = torch.empty(inp["N"], H, dtype=torch.bfloat16, device=dev)
+    bufs = pl.make_chunk_buffers(T, E, K, H, R, ep.EP_DTYPE_FP8_E4M3_B128, dev)
     offs = inp["rank_offsets"].cpu().tolist()
-    halves = []
-    for lo, hi in ((0, R // 2), (R // 2, R)):
-        t0, t1 = offs[lo], offs[hi]
-        n = t1 - t0
-        d = dict(n=n, logits=inp["logits"][t0:t1], x=inp["x"][t0:t1],
-                 y=inp["y"][t0 * K:t1 * K],
-                 ro=(inp["rank_offsets"][lo:hi + 1] - t0).contiguous(),
-                 idx=torch.empty(n, K, dtype=torch.int32, device=dev),
-                 wt=torch.empty(n, K, dtype=torch.float32, device=dev),
-                 lay=ep.alloc_layout(n, E, K, hi - lo, 0, dev),
-                 ws=torch.empty(ep.ep_dispatch_layout_workspace_size(n, E, K, hi - lo),
-                                dtype=torch.uint8, device=dev),
-                 q=torch.empty(n * K, H, dtype=torch.uint8, device=dev),
-                 qs=torch.empty(n * K, H // 128, dtype=torch.float32, device=dev),
-                 comb=torch.empty(n, H, dtype=torch.bfloat16, device=dev),
-                 s=torch.cuda.Stream(device=dev))
-        halves.append(d)
+    ro_rounds = pl.chunk_rank_offsets(offs, inp["N"], T, dev)
+    y = inp["y"]
 
-    def run_half(d):
-        with torch.cuda.stream(d["s"]):
-            ep.ep_route_topk(d["logits"], K, topk_idx=d["idx"], topk_w=d["wt"])
-            ep.ep_dispatch_layout(d["idx"], d["ro"], E, 0, out=d["lay"], workspace=d["ws"])
-            ep.ep_dispatch(d["x"], d["idx"], d["lay"].pos, d["lay"].expert_offsets, E,
-                           ep.EP_LAYOUT_CONTIG, 0, ep.EP_DTYPE_FP8_E4M3_B128, out=d["q"],
-                           out_scales=d["qs"])
-            ep.ep_combine(d["y"], d["idx"], d["wt"], d["lay"].pos, d["lay"].expert_offsets, E,
-                          ep.EP_LAYOUT_CONTIG, 0, out=d["comb"])
+    def step():
+        pl.chunked(inp["logits"], inp["x"], offs, K, ep.EP_DTYPE_FP8_E4M3_B128, bufs,
+                   lambda t0, n, out, sc, lay: y[t0 * K:(t0 + n) * K], comb,
+                   ro_rounds=ro_rounds)
 
-    def step(ev=None):
-        if ev:
-            ev[0].record(main_stream)
-        for d in halves:
-            d["s"].wait_stream(main_stream)
-        for d in halves:
-            run_half(d)
-        for d in halves:
-            main_stream.wait_stream(d["s"])
-        if ev:
-            ev[1].record(main_stream)
+    res = _time_schedule(args, torch, main_stream, flush, dist, step, inp["N"],
+                         f"rounds of {T} tokens")
+    res["dispatch_buffer_bytes"] = bufs.dispatch_bytes
+    res["dispatch_buffer_bytes_unchunked"] = inp["N"] * K * (H + H // 128 * 4)
+    return res
 
+
+def _time_schedule(args, torch, main_stream, flush, dist, step, N, note):
     for i in range(args.warmup):
         flush.fill_(i & 0xFF)
         step()
@@ -433,14 +430,14 @@ def two_batch_overlap(args, ep, torch, dev, main_stream, inp, w, flush, dist):
     barrier(dist)
     for i in range(steps):
         flush.fill_((i + 3) & 0xFF)
-        step(evs[i])
+        evs[i][0].record(main_stream)
+        step()
+        evs[i][1].record(main_stream)
     torch.cuda.synchronize()
     total = max_over_ranks(dist, sum(e[0].elapsed_time(e[1]) for e in evs))
     world = 1 if dist is None else dist.get_world_size()
-    tok = inp["N"] * world
-    return {"tokens_per_s": round(tok * steps / (total / 1e3), 1),
-            "ms_per_step": round(total / steps, 4), "steps": steps,
-            "note": "ranks 0..3 and 4..7 as two micro-batches on two streams"}
+    return {"tokens_per_s": round(N * world * steps / (total / 1e3), 1),
+            "ms_per_step": round(total / steps, 4), "steps": steps, "note": note}
 
 
 def decode_latency(args, ep, torch, dev, stream, flush):

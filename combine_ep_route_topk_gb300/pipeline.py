@@ -1,0 +1,179 @@
+"""Schedules of the EP path built from the library's entry points.
+
+two_batch_overlap
+    "21K output tokens/s DeepSeek inference on MI300X", "Computation-
+    communication overlapping", and "Expert Parallelism" (SGLang docs),
+    "Two-Batch Overlap": the batch is split into two micro-batches whose
+    stages run on two streams, so one micro-batch's latency-bound routing and
+    layout overlap the other's HBM-bound dispatch and combine.  On one GPU the
+    micro-batches are the first and second half of the logical ranks; each
+    has its own expert-major layout.
+
+chunked
+    "Expert Parallelism" (SGLang docs), "Ascend NPU guidance", the ant-moving
+    function: a long sequence is sent in rounds of a fixed number of tokens,
+    so the dispatch buffer is bounded by round_tokens * K rows instead of
+    N * K.  Each round routes, lays out and dispatches its tokens, hands the
+    dispatched rows to the caller's expert function, and combines the
+    result into the round's slice of the output.
+
+Both only call the C ABI through the binding (every step runs in the
+library's kernels); the host work is slicing and stream ordering.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import ep as _ep
+
+
+@dataclass
+class MicroBatch:
+    """Views and buffers of one micro-batch (tokens [t0, t1) of the batch)."""
+    t0: int
+    t1: int
+    logits: torch.Tensor
+    x: torch.Tensor
+    ro: torch.Tensor            # rank offsets relative to t0, on the device
+    idx: torch.Tensor
+    wt: torch.Tensor
+    lay: _ep.Layout
+    ws: torch.Tensor
+    out: torch.Tensor           # dispatched rows (bf16 or FP8 codes)
+    scales: torch.Tensor | None
+    comb: torch.Tensor          # view into the combined output
+    stream: torch.cuda.Stream
+
+
+def split_by_ranks(rank_offsets_host, parts=2):
+    """Contiguous rank groups: [(rank_lo, rank_hi)], ranks split evenly."""
+    R = len(rank_offsets_host) - 1
+    bounds = [round(i * R / parts) for i in range(parts + 1)]
+    return [(bounds[i], bounds[i + 1]) for i in range(parts) if bounds[i] < bounds[i + 1]]
+
+
+def make_micro_batches(logits, x, rank_offsets, K, dtype, comb, parts=2):
+    """Buffers for `parts` micro-batches of contiguous rank groups."""
+    dev = logits.device
+    E = logits.shape[1]
+    H = x.shape[1]
+    offs = rank_offsets.cpu().tolist()
+    mbs = []
+    for lo, hi in split_by_ranks(offs, parts):
+        t0, t1 = offs[lo], offs[hi]
+        n = t1 - t0
+        ro = torch.tensor([o - t0 for o in offs[lo:hi + 1]], dtype=torch.int32, device=dev)
+        fp8 = dtype == _ep.EP_DTYPE_FP8_E4M3_B128
+        mbs.append(MicroBatch(
+            t0=t0, t1=t1, logits=logits[t0:t1], x=x[t0:t1], ro=ro,
+            idx=torch.empty(n, K, dtype=torch.int32, device=dev),
+            wt=torch.empty(n, K, dtype=torch.float32, device=dev),
+            lay=_ep.alloc_layout(n, E, K, hi - lo, 0, dev),
+            ws=torch.empty(_ep.ep_dispatch_layout_workspace_size(n, E, K, hi - lo),
+                           dtype=torch.uint8, device=dev),
+            out=torch.empty(n * K, H, dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev),
+            scales=torch.empty(n * K, H // 128, dtype=torch.float32, device=dev) if fp8 else None,
+            comb=comb[t0:t1], stream=torch.cuda.Stream(device=dev)))
+    return mbs
+
+
+def two_batch_overlap(mbs, K, dtype, expert_out, main_stream=None):
+    """Run route -> layout -> dispatch -> combine for every micro-batch on its
+    own stream; `expert_out(mb)` returns the bf16 expert outputs [rows, H] for
+    the micro-batch (called on its stream after its dispatch).  The calling
+    stream waits for all micro-batches at the end."""
+    main = torch.cuda.current_stream() if main_stream is None else main_stream
+    for mb in mbs:
+        mb.stream.wait_stream(main)
+    for mb in mbs:
+        with torch.cuda.stream(mb.stream):
+            E = mb.logits.shape[1]
+            _ep.ep_route_topk(mb.logits, K, topk_idx=mb.idx, topk_w=mb.wt)
+            _ep.ep_dispatch_layout(mb.idx, mb.ro, E, 0, out=mb.lay, workspace=mb.ws)
+            _ep.ep_dispatch(mb.x, mb.idx, mb.lay.pos, mb.lay.expert_offsets, E,
+                            _ep.EP_LAYOUT_CONTIG, 0, dtype, out=mb.out, out_scales=mb.scales)
+            y = expert_out(mb)
+            _ep.ep_combine(y, mb.idx, mb.wt, mb.lay.pos, mb.lay.expert_offsets, E,
+                           _ep.EP_LAYOUT_CONTIG, 0, out=mb.comb)
+    for mb in mbs:
+        main.wait_stream(mb.stream)
+
+
+@dataclass
+class ChunkBuffers:
+    """Round-sized buffers: the dispatch buffer holds round_tokens * K rows."""
+    round_tokens: int
+    idx: torch.Tensor
+    wt: torch.Tensor
+    ws: torch.Tensor
+    out: torch.Tensor
+    scales: torch.Tensor | None
+
+    @property
+    def dispatch_bytes(self) -> int:
+        b = self.out.numel() * self.out.element_size()
+        if self.scales is not None:
+            b += self.scales.numel() * 4
+        return b
+
+
+def make_chunk_buffers(round_tokens, E, K, H, R, dtype, device):
+    fp8 = dtype == _ep.EP_DTYPE_FP8_E4M3_B128
+    T = round_tokens
+    return ChunkBuffers(
+        round_tokens=T,
+        idx=torch.empty(T, K, dtype=torch.int32, device=device),
+        wt=torch.empty(T, K, dtype=torch.float32, device=device),
+        ws=torch.empty(_ep.ep_dispatch_layout_workspace_size(T, E, K, R), dtype=torch.uint8,
+                       device=device),
+        out=torch.empty(T * K, H, dtype=torch.uint8 if fp8 else torch.bfloat16, device=device),
+        scales=torch.empty(T * K, H // 128, dtype=torch.float32, device=device) if fp8 else None)
+
+
+def round_rank_offsets(rank_offsets_host, t0, t1):
+    """Rank offsets of the round [t0, t1): each rank's tokens clipped to the
+    round, relative to t0 (ranks with no token in the round are empty)."""
+    return [min(max(o, t0), t1) - t0 for o in rank_offsets_host]
+
+
+def chunk_rank_offsets(rank_offsets_host, N, T, device):
+    """Device tensor [rounds, R+1] of every round's rank offsets."""
+    R = len(rank_offsets_host) - 1
+    starts = list(range(0, N, T))
+    return torch.tensor([round_rank_offsets(rank_offsets_host, t0, min(N, t0 + T))
+                         for t0 in starts], dtype=torch.int32).reshape(len(starts),
+                                                                      R + 1).to(device)
+
+
+def chunked(logits, x, rank_offsets_host, K, dtype, bufs: ChunkBuffers, expert_out, comb,
+            ro_rounds=None):
+    """Ant-moving rounds over the packed token sequence.  `expert_out(r0, n,
+    out_rows, scales, layout)` returns the bf16 expert outputs [n*K, H] of the
+    round's dispatched rows.  Results land in comb[t0:t1] for each round.
+    `ro_rounds` (chunk_rank_offsets) may be passed to skip the upload.
+    Returns [(t0, t1, layout)] per round (the layouts for inspection)."""
+    N, E = logits.shape
+    T = bufs.round_tokens
+    starts = list(range(0, N, T))
+    # every round's rank offsets in one upload, before the first launch
+    ro_all = ro_rounds if ro_rounds is not None else \
+        chunk_rank_offsets(rank_offsets_host, N, T, logits.device)
+    rounds = []
+    for j, t0 in enumerate(starts):
+        t1 = min(N, t0 + T)
+        n = t1 - t0
+        ro = ro_all[j]
+        idx, wt = bufs.idx[:n], bufs.wt[:n]
+        _ep.ep_route_topk(logits[t0:t1], K, topk_idx=idx, topk_w=wt)
+        lay = _ep.ep_dispatch_layout(idx, ro, E, 0, workspace=bufs.ws)
+        out = bufs.out[:n * K]
+        scales = None if bufs.scales is None else bufs.scales[:n * K]
+        _ep.ep_dispatch(x[t0:t1], idx, lay.pos, lay.expert_offsets, E, _ep.EP_LAYOUT_CONTIG, 0,
+                        dtype, out=out, out_scales=scales)
+        y = expert_out(t0, n, out, scales, lay)
+        _ep.ep_combine(y, idx, wt, lay.pos, lay.expert_offsets, E, _ep.EP_LAYOUT_CONTIG, 0,
+                       out=comb[t0:t1])
+        rounds.append((t0, t1, lay))
+    return rounds
