@@ -261,10 +261,12 @@ def run_ours(args, world, rank, local):
     if int(status.item()) != 0:
         raise RuntimeError("route+layout kernel reported a barrier timeout")
 
-    overlap = two_batch_overlap(args, ep, torch, dev, stream, inp, w, flush, dist)
-    chunk = chunked_prefill(args, ep, torch, dev, stream, inp, w, flush, dist,
-                            T=min(8192, max(8, inp["N"] // 4)))
-    decode = decode_latency(args, ep, torch, dev, stream, flush) if rank == 0 else None
+    overlap = chunk = decode = None
+    if not args.no_extras:
+        overlap = two_batch_overlap(args, ep, torch, dev, stream, inp, w, flush, dist)
+        chunk = chunked_prefill(args, ep, torch, dev, stream, inp, w, flush, dist,
+                                T=min(8192, max(8, inp["N"] // 4)))
+        decode = decode_latency(args, ep, torch, dev, stream, flush) if rank == 0 else None
 
     stage = {n: [e[j].elapsed_time(e[j + 1]) for e in evs]
              for j, n in enumerate(["route", "layout", "dispatch", "combine"])}
@@ -592,6 +594,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--fused", action="store_true",
                     help="route + layout as the one cooperative kernel (ep_route_layout)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the overlap, chunked and decode measurements (profiling)")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode step (for profiling its kernels)")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
