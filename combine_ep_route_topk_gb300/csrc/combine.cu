@@ -47,6 +47,7 @@ template <int NT, int KC>
 __global__ void __launch_bounds__(NT) combine_kernel(MoveArgs a) {
     __shared__ long long s_row[kMaxK];
     __shared__ float s_w[kMaxK];
+    pdl_prologue();
     const int t = blockIdx.x;
     const int K = KC > 0 ? KC : a.K;
     if (threadIdx.x < K) {
@@ -90,15 +91,16 @@ __global__ void __launch_bounds__(NT) combine_kernel(MoveArgs a) {
 
 cudaError_t launch_combine(const MoveArgs& a, cudaStream_t s) {
     if (a.N == 0) return cudaSuccess;
+    cudaError_t err;
     switch (a.K) {
-        case 1: combine_kernel<128, 1><<<a.N, 128, 0, s>>>(a); break;
-        case 2: combine_kernel<128, 2><<<a.N, 128, 0, s>>>(a); break;
-        case 4: combine_kernel<128, 4><<<a.N, 128, 0, s>>>(a); break;
-        case 8: combine_kernel<128, 8><<<a.N, 128, 0, s>>>(a); break;
-        default: combine_kernel<128, 0><<<a.N, 128, 0, s>>>(a); break;
+        case 1: err = launch(combine_kernel<128, 1>, dim3(a.N), dim3(128), 0, s, a); break;
+        case 2: err = launch(combine_kernel<128, 2>, dim3(a.N), dim3(128), 0, s, a); break;
+        case 4: err = launch(combine_kernel<128, 4>, dim3(a.N), dim3(128), 0, s, a); break;
+        case 8: err = launch(combine_kernel<128, 8>, dim3(a.N), dim3(128), 0, s, a); break;
+        default: err = launch(combine_kernel<128, 0>, dim3(a.N), dim3(128), 0, s, a); break;
     }
     note_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace ep

@@ -37,6 +37,7 @@ __device__ __forceinline__ long long dest_row(const MoveArgs& a, int t, int k) {
 template <int NT, int U>
 __global__ void __launch_bounds__(NT) dispatch_bf16_kernel(MoveArgs a) {
     __shared__ long long s_dst[kMaxK];
+    pdl_prologue();
     const int t = blockIdx.x;
     if (threadIdx.x < a.K) s_dst[threadIdx.x] = dest_row(a, t, threadIdx.x);
     __syncthreads();
@@ -96,6 +97,7 @@ __device__ __forceinline__ float amax16(const uint4& lo, const uint4& hi) {
 template <int NT, int U>
 __global__ void __launch_bounds__(NT) dispatch_fp8_kernel(MoveArgs a) {
     __shared__ long long s_dst[kMaxK];
+    pdl_prologue();
     const int t = blockIdx.x;
     if (threadIdx.x < a.K) s_dst[threadIdx.x] = dest_row(a, t, threadIdx.x);
     __syncthreads();
@@ -150,10 +152,11 @@ __global__ void __launch_bounds__(NT) dispatch_fp8_kernel(MoveArgs a) {
 
 cudaError_t launch_dispatch(const MoveArgs& a, cudaStream_t s) {
     if (a.N == 0) return cudaSuccess;
-    if (a.dtype == 0) dispatch_bf16_kernel<128, 8><<<a.N, 128, 0, s>>>(a);
-    else dispatch_fp8_kernel<128, 2><<<a.N, 128, 0, s>>>(a);
+    const cudaError_t err =
+        a.dtype == 0 ? launch(dispatch_bf16_kernel<128, 8>, dim3(a.N), dim3(128), 0, s, a)
+                     : launch(dispatch_fp8_kernel<128, 2>, dim3(a.N), dim3(128), 0, s, a);
     note_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace ep

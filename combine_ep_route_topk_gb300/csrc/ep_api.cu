@@ -3,6 +3,7 @@
 // synchronises or reads device memory.
 #include <atomic>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "ep.h"
@@ -48,6 +49,14 @@ int sm_count() {
 }
 
 void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("EP_DISABLE_PDL");
+        return !(v && v[0] == '1');
+    }();
+    return on;
+}
 
 }  // namespace ep
 

@@ -16,6 +16,39 @@ constexpr int kMaxR = 1024;
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
+// ---- programmatic dependent launch -----------------------------------------
+// Every kernel of the library starts with pdl_prologue(): it waits until the
+// grids it depends on in the stream have completed and their writes are
+// visible (griddepcontrol.wait, before any global load or store), then allows
+// the next kernel of the stream to be launched (griddepcontrol.launch_
+// dependents).  Kernels are launched with programmatic stream serialisation,
+// so the next kernel's blocks are scheduled while this kernel's last wave
+// runs and start their work the moment it ends, instead of after a launch
+// gap.  Stream order and results are unchanged.  EP_DISABLE_PDL=1 in the
+// environment turns the launch attribute off (plain stream order).
+__device__ __forceinline__ void pdl_prologue() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+bool pdl_enabled();
+
+template <typename... Params, typename... Args>
+cudaError_t launch(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                   Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
 // Counts one kernel launch (ep_kernel_launch_count).
 void note_launch(int n = 1);
 

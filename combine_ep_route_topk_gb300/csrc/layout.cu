@@ -44,6 +44,7 @@ using namespace lay;
 
 // ---- 1. chunk histograms --------------------------------------------------
 __global__ void __launch_bounds__(kNT) layout_hist_kernel(LayoutArgs a, int C) {
+    pdl_prologue();
     extern __shared__ int smem[];
     int* s_m = smem;
     int* s_tab = s_m + round_up4(a.R + 1);
@@ -73,6 +74,7 @@ __global__ void __launch_bounds__(kNT) layout_hist_kernel(LayoutArgs a, int C) {
 
 // ---- 2. column scans --------------------------------------------------------
 __global__ void __launch_bounds__(1024) layout_scan_kernel(LayoutArgs a, int C) {
+    pdl_prologue();
     extern __shared__ int smem[];
     int* s_m = smem;
     int* s_tab = s_m + round_up4(a.R + 1);
@@ -126,6 +128,7 @@ __global__ void __launch_bounds__(1024) layout_scan_kernel(LayoutArgs a, int C) 
 
 // ---- 3. stable scatter of positions ----------------------------------------
 __global__ void __launch_bounds__(kNT) layout_scatter_kernel(LayoutArgs a, int C) {
+    pdl_prologue();
     extern __shared__ int smem[];
     int* s_m = smem;
     int* s_tab = s_m + round_up4(a.R + 1);
@@ -148,11 +151,13 @@ cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t s) {
     const size_t sh_hist = (size_t)(tab + a.E) * sizeof(int);
     const size_t sh_scan = (size_t)(tab + 1024 + 32) * sizeof(int);
     const size_t sh_scat = (size_t)(tab + ((a.E + 1 + 3) & ~3) + kWarps * a.E) * sizeof(int);
-    layout_hist_kernel<<<slots, kNT, sh_hist, s>>>(a, C);
-    layout_scan_kernel<<<(a.E + 31) / 32, 1024, sh_scan, s>>>(a, C);
-    layout_scatter_kernel<<<slots, kNT, sh_scat, s>>>(a, C);
+    cudaError_t err = launch(layout_hist_kernel, dim3(slots), dim3(kNT), sh_hist, s, a, C);
+    if (err == cudaSuccess)
+        err = launch(layout_scan_kernel, dim3((a.E + 31) / 32), dim3(1024), sh_scan, s, a, C);
+    if (err == cudaSuccess)
+        err = launch(layout_scatter_kernel, dim3(slots), dim3(kNT), sh_scat, s, a, C);
     note_launch(3);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace ep

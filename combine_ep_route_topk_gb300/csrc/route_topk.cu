@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(256)
 route_topk_kernel(const float* __restrict__ logits, int N, int E, int Kr,
                   const int32_t* __restrict__ emap, int32_t* __restrict__ topk_idx,
                   float* __restrict__ topk_w) {
+    pdl_prologue();
     const int K = KT > 0 ? KT : Kr;
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -38,14 +39,14 @@ route_topk_kernel(const float* __restrict__ logits, int N, int E, int Kr,
 }
 
 template <int VPL, bool VEC>
-void launch_route(const float* logits, int N, int E, int K, const int32_t* emap,
-                  int32_t* idx, float* w, cudaStream_t s) {
-    const int blocks = (N + 7) / 8;
+cudaError_t launch_route(const float* logits, int N, int E, int K, const int32_t* emap,
+                         int32_t* idx, float* w, cudaStream_t s) {
+    const dim3 grid((N + 7) / 8), block(256);
     switch (K) {
-        case 2: route_topk_kernel<VPL, VEC, 2><<<blocks, 256, 0, s>>>(logits, N, E, K, emap, idx, w); break;
-        case 4: route_topk_kernel<VPL, VEC, 4><<<blocks, 256, 0, s>>>(logits, N, E, K, emap, idx, w); break;
-        case 8: route_topk_kernel<VPL, VEC, 8><<<blocks, 256, 0, s>>>(logits, N, E, K, emap, idx, w); break;
-        default: route_topk_kernel<VPL, VEC, 0><<<blocks, 256, 0, s>>>(logits, N, E, K, emap, idx, w); break;
+        case 2: return launch(route_topk_kernel<VPL, VEC, 2>, grid, block, 0, s, logits, N, E, K, emap, idx, w);
+        case 4: return launch(route_topk_kernel<VPL, VEC, 4>, grid, block, 0, s, logits, N, E, K, emap, idx, w);
+        case 8: return launch(route_topk_kernel<VPL, VEC, 8>, grid, block, 0, s, logits, N, E, K, emap, idx, w);
+        default: return launch(route_topk_kernel<VPL, VEC, 0>, grid, block, 0, s, logits, N, E, K, emap, idx, w);
     }
 }
 
@@ -53,6 +54,7 @@ void launch_route(const float* logits, int N, int E, int K, const int32_t* emap,
 
 __global__ void __launch_bounds__(1024)
 balance_map_kernel(const int32_t* __restrict__ counts, int R, int E, int32_t* __restrict__ emap) {
+    pdl_prologue();
     __shared__ unsigned long long s_key[kMaxE];
     __shared__ long long s_load[kMaxR];
     __shared__ int s_size[kMaxR];
@@ -135,33 +137,27 @@ cudaError_t launch_route_topk(const float* logits, int N, int E, int K, const in
                               int32_t* idx, float* w, cudaStream_t s) {
     if (N == 0) return cudaSuccess;
     const bool vec = (E % 128 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
-    if (vec) {
-        switch (E) {
-            case 128: launch_route<4, true>(logits, N, E, K, emap, idx, w, s); break;
-            case 256: launch_route<8, true>(logits, N, E, K, emap, idx, w, s); break;
-            case 512: launch_route<16, true>(logits, N, E, K, emap, idx, w, s); break;
-            case 1024: launch_route<32, true>(logits, N, E, K, emap, idx, w, s); break;
-            default: goto scalar;
-        }
-        note_launch();
-        return cudaGetLastError();
-    }
-scalar:
-    if (E <= 32) launch_route<1, false>(logits, N, E, K, emap, idx, w, s);
-    else if (E <= 64) launch_route<2, false>(logits, N, E, K, emap, idx, w, s);
-    else if (E <= 128) launch_route<4, false>(logits, N, E, K, emap, idx, w, s);
-    else if (E <= 256) launch_route<8, false>(logits, N, E, K, emap, idx, w, s);
-    else if (E <= 512) launch_route<16, false>(logits, N, E, K, emap, idx, w, s);
-    else launch_route<32, false>(logits, N, E, K, emap, idx, w, s);
+    cudaError_t err;
+    if (vec && E == 128) err = launch_route<4, true>(logits, N, E, K, emap, idx, w, s);
+    else if (vec && E == 256) err = launch_route<8, true>(logits, N, E, K, emap, idx, w, s);
+    else if (vec && E == 512) err = launch_route<16, true>(logits, N, E, K, emap, idx, w, s);
+    else if (vec && E == 1024) err = launch_route<32, true>(logits, N, E, K, emap, idx, w, s);
+    else if (E <= 32) err = launch_route<1, false>(logits, N, E, K, emap, idx, w, s);
+    else if (E <= 64) err = launch_route<2, false>(logits, N, E, K, emap, idx, w, s);
+    else if (E <= 128) err = launch_route<4, false>(logits, N, E, K, emap, idx, w, s);
+    else if (E <= 256) err = launch_route<8, false>(logits, N, E, K, emap, idx, w, s);
+    else if (E <= 512) err = launch_route<16, false>(logits, N, E, K, emap, idx, w, s);
+    else err = launch_route<32, false>(logits, N, E, K, emap, idx, w, s);
     note_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 cudaError_t launch_balance_map(const int32_t* counts, int R, int E, int32_t* emap,
                                cudaStream_t s) {
-    balance_map_kernel<<<1, 1024, 0, s>>>(counts, R, E, emap);
+    const cudaError_t err = launch(balance_map_kernel, dim3(1), dim3(1024), 0, s, counts, R, E,
+                                   emap);
     note_launch();
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace ep
