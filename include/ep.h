@@ -42,6 +42,14 @@
  *     [0,E), rank_offsets that are not a non-decreasing 0..N sequence, pos
  *     values that do not come from ep_dispatch_layout) never cause an access
  *     outside the buffers described here: such picks are skipped.
+ *   - Kernels are launched with programmatic dependent launch: each one waits
+ *     for the preceding grids of the stream to complete (griddepcontrol.wait)
+ *     before touching memory, then lets the next kernel launch early.  A
+ *     caller kernel that follows ours and is itself launched with the
+ *     programmatic-serialisation attribute must wait for its grid dependency
+ *     (cudaGridDependencySynchronize) before reading our outputs; kernels
+ *     launched without it see plain stream order.  EP_DISABLE_PDL=1 in the
+ *     environment launches ours without the attribute.
  *   - bf16 is IEEE binary16-brain (1-8-7); FP8 is OCP E4M3FN.
  *   - Limits: 1 <= E <= 1024, 1 <= K <= min(E, 32), 1 <= R <= 1024,
  *     0 <= N, N*K <= 2^31 - 1; beyond them EP_ERR_UNSUPPORTED.
