@@ -36,8 +36,9 @@
  *   - Arguments are checked on the host before anything is launched; a bad
  *     argument returns EP_ERR_INVALID_ARG (or EP_ERR_WORKSPACE /
  *     EP_ERR_UNSUPPORTED) and launches nothing.  A failed launch returns
- *     EP_ERR_CUDA.  No kernel traps, asserts or waits on another kernel; the
- *     only waits are the bounded grid barriers inside ep_route_layout.
+ *     EP_ERR_CUDA.  No kernel traps or asserts.  Besides the stream-order wait
+ *     of programmatic launch (below), the only waits are the bounded grid
+ *     barriers inside ep_route_layout.
  *   - Device-side data that break a precondition (an expert id outside
  *     [0,E), rank_offsets that are not a non-decreasing 0..N sequence, pos
  *     values that do not come from ep_dispatch_layout) never cause an access
