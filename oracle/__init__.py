@@ -38,7 +38,8 @@ DTYPE_FP8 = 1
 def _lib():
     global _LIB
     if _LIB is None:
-        path = _build.build()
+        # EP_ORACLE_LIB lets the mutation tests load a deliberately broken copy
+        path = os.environ.get("EP_ORACLE_LIB") or _build.build()
         lib = ctypes.CDLL(path)
         P = ctypes.c_void_p
         i32, i64 = ctypes.c_int32, ctypes.c_int64

@@ -438,3 +438,28 @@ def test_combine_masked_drops_overflow_picks():
     out = oracle.bf16_to_float(oracle.combine(y, idx, w, lay["pos"], lay["expert_offsets"], E,
                                               layout=oracle.LAYOUT_MASKED, cap=cap))
     assert np.all(out[:cap] == 1.0) and np.all(out[cap:] == 0.0)
+
+
+def test_combine_float_chain_rounding_fixtures():
+    """Hand-computed: the fp32 FMA chain in pick order k = 0..K-1 decides a bf16
+    rounding tie.  Picks (w, y) = (1, 1), (2^-8, 1), (2^-24, 1), (2^-24, 1):
+    in order the float sum stays at 1 + 2^-8 (each 2^-24 is a tie that rounds
+    to even), which is a bf16 midpoint and rounds to even: 1.0 (0x3F80).
+    Summed in reverse order (2^-24 + 2^-24 + 2^-8 + 1 = 1 + 2^-8 + 2^-23,
+    exact in float) or in double, the value is above the midpoint: 1 + 2^-7."""
+    N, E, K, H = 1, 4, 4, 8
+    idx = np.array([[0, 1, 2, 3]], np.int32)
+    w = np.array([[1.0, 2.0 ** -8, 2.0 ** -24, 2.0 ** -24]], np.float32)
+    lay = oracle.layout(idx, np.array([0, 1], np.int32), E)
+    y = oracle.float_to_bf16(np.ones(K * H, np.float32)).reshape(K, H)
+    out = oracle.combine(y, idx, w, lay["pos"], lay["expert_offsets"], E)
+    assert np.all(out == 0x3F80)
+    # picks (1, 1) and (2^-8 + 2^-30, 1): float keeps 1 + 2^-8 (the 2^-30 is
+    # below half an ulp), a bf16 tie -> 1.0; accumulated in double the value
+    # stays above the midpoint and would round up to 1 + 2^-7 (0x3F81)
+    w2 = np.array([[1.0, 2.0 ** -8 + 2.0 ** -30]], np.float32)
+    assert float(w2[0, 1]) == 2.0 ** -8 + 2.0 ** -30
+    idx2 = np.array([[0, 1]], np.int32)
+    lay2 = oracle.layout(idx2, np.array([0, 1], np.int32), 2)
+    out2 = oracle.combine(y[:2], idx2, w2, lay2["pos"], lay2["expert_offsets"], 2)
+    assert np.all(out2 == 0x3F80)
