@@ -154,7 +154,7 @@ cudaError_t launch_dispatch(const MoveArgs& a, cudaStream_t s) {
     if (a.N == 0) return cudaSuccess;
     const cudaError_t err =
         a.dtype == 0 ? launch(dispatch_bf16_kernel<128, 8>, dim3(a.N), dim3(128), 0, s, a)
-                     : launch(dispatch_fp8_kernel<128, 2>, dim3(a.N), dim3(128), 0, s, a);
+                     : launch(dispatch_fp8_kernel<256, 2>, dim3(a.N), dim3(256), 0, s, a);
     note_launch();
     return err;
 }
