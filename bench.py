@@ -153,6 +153,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def describe_workload(w, N):
+    return (f"{w.R} logical ranks, {N} tokens, E={w.E}, K={w.K}, H={w.H}, "
+            f"{'FP8 E4M3 1x128' if w.dtype else 'bf16'} "
+            f"{'masked (capacity %d)' % w.cap if w.layout else 'contiguous'} dispatch, "
+            f"bf16 combine" + (", experts renumbered by the balanced partition"
+                               if w.relabel else ""))
+
+
 def gpu_smi_id(local: int) -> str:
     """nvidia-smi --id for this process's CUDA device (its UUID when known)."""
     import torch
@@ -168,16 +176,19 @@ def gpu_smi_id(local: int) -> str:
     return str(local)
 
 
-def byte_model(N, E, K, H):
-    """Algorithmic bytes per launch (the minimum each kernel must move)."""
-    sb = H // 128 * 4
+def byte_model(N, E, K, H, fp8=True, delivered=None):
+    """Algorithmic bytes per launch (the minimum each kernel must move).
+    `delivered` rows are written by dispatch and read by combine (N*K for
+    the contiguous layout; the masked layout drops picks past capacity)."""
+    D = N * K if delivered is None else delivered
+    row_out = (H + H // 128 * 4) if fp8 else H * 2
     return {
         "route": N * E * 4 + N * K * 8,
         "layout": N * K * 4 + N * K * 8,
-        "dispatch": N * H * 2 + N * K * (H + sb) + N * K * 8,
-        "combine": N * K * H * 2 + N * H * 2 + N * K * 12,
+        "dispatch": N * H * 2 + D * row_out + N * K * 8,
+        "combine": D * H * 2 + N * H * 2 + N * K * 12,
         # each pick counted as a full row read and a row written
-        "dispatch_rowwise": N * K * H * 2 + N * K * (H + sb),
+        "dispatch_rowwise": D * H * 2 + D * row_out,
     }
 
 
@@ -191,22 +202,27 @@ def run_ours(args, world, rank, local):
     dist = init_dist(world)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = wl.WORKLOADS["prefill"]
+    w = wl.WORKLOADS[args.workload]
     if args.tokens_per_rank:  # smaller case of the same workload (profiling)
         w = w.scaled(batch=("fixed", args.tokens_per_rank))
     inp = wl.make_inputs(w, seed=args.seed + rank, device=str(dev))
     N, E, K, H, R = inp["N"], w.E, w.K, w.H, w.R
     logits, ro, x, y = inp["logits"], inp["rank_offsets"], inp["x"], inp["y"]
+    layout = w.layout
+    cap = w.cap if layout == ep.EP_LAYOUT_MASKED else 0
+    dtype = w.dtype
+    rows = N * K if layout == ep.EP_LAYOUT_CONTIG else E * cap
 
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
     idx = torch.empty(N, K, dtype=torch.int32, device=dev)
     wt = torch.empty(N, K, dtype=torch.float32, device=dev)
-    lay = ep.alloc_layout(N, E, K, R, 0, dev)
+    lay = ep.alloc_layout(N, E, K, R, cap, dev)
     ws = torch.empty(ep.ep_dispatch_layout_workspace_size(N, E, K, R), dtype=torch.uint8,
                      device=dev)
-    q = torch.empty(N * K, H, dtype=torch.uint8, device=dev)
-    qs = torch.empty(N * K, H // 128, dtype=torch.float32, device=dev)
+    fp8 = dtype == ep.EP_DTYPE_FP8_E4M3_B128
+    q = torch.empty(rows, H, dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    qs = torch.empty(rows, H // 128, dtype=torch.float32, device=dev) if fp8 else None
     comb = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
@@ -214,28 +230,31 @@ def run_ours(args, world, rank, local):
     ws_fused = torch.empty(ep.ep_route_layout_workspace_size(N, E, K, R), dtype=torch.uint8,
                            device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    emap = None
+    if w.relabel:  # balanced renumbering measured on this batch (before timing)
+        i0, _ = ep.ep_route_topk(logits, K)
+        emap = ep.ep_expert_balance_map(ep.ep_dispatch_layout(i0, ro, E).counts)
 
     def step(ev=None):
         if ev:
             ev[0].record(stream)
         if fused:  # route + layout in one cooperative kernel
-            ep.ep_route_layout(logits, ro, K, 0, topk_idx=idx, topk_w=wt, out=lay,
-                               status=status, workspace=ws_fused)
+            ep.ep_route_layout(logits, ro, K, cap, expert_map=emap, topk_idx=idx, topk_w=wt,
+                               out=lay, status=status, workspace=ws_fused)
             if ev:
                 ev[1].record(stream)
         else:
-            ep.ep_route_topk(logits, K, topk_idx=idx, topk_w=wt)
+            ep.ep_route_topk(logits, K, expert_map=emap, topk_idx=idx, topk_w=wt)
             if ev:
                 ev[1].record(stream)
-            ep.ep_dispatch_layout(idx, ro, E, 0, out=lay, workspace=ws)
+            ep.ep_dispatch_layout(idx, ro, E, cap, out=lay, workspace=ws)
         if ev:
             ev[2].record(stream)
-        ep.ep_dispatch(x, idx, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_CONTIG, 0,
-                       ep.EP_DTYPE_FP8_E4M3_B128, out=q, out_scales=qs)
+        ep.ep_dispatch(x, idx, lay.pos, lay.expert_offsets, E, layout, cap, dtype, out=q,
+                       out_scales=qs)
         if ev:
             ev[3].record(stream)
-        ep.ep_combine(y, idx, wt, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_CONTIG, 0,
-                      out=comb)
+        ep.ep_combine(y, idx, wt, lay.pos, lay.expert_offsets, E, layout, cap, out=comb)
         if ev:
             ev[4].record(stream)
 
@@ -243,6 +262,7 @@ def run_ours(args, world, rank, local):
         flush.fill_(i & 0xFF)
         step()
     torch.cuda.synchronize()
+    delivered = N * K if layout == ep.EP_LAYOUT_CONTIG else int(lay.masked_m.sum().item())
 
     # timed region: one event pair per step, nothing between the kernels (an
     # event between two kernels would keep the second from launching early)
@@ -274,7 +294,7 @@ def run_ours(args, world, rank, local):
         raise RuntimeError("route+layout kernel reported a barrier timeout")
 
     overlap = chunk = decode = None
-    if not args.no_extras:
+    if not args.no_extras and args.workload == "prefill":
         overlap = two_batch_overlap(args, ep, torch, dev, stream, inp, w, flush, dist)
         chunk = chunked_prefill(args, ep, torch, dev, stream, inp, w, flush, dist,
                                 T=min(8192, max(8, inp["N"] // 4)))
@@ -325,7 +345,7 @@ def run_ours(args, world, rank, local):
     tok = N * world
     ms_per_step = total_ms / steps
     value = tok * steps / (total_ms / 1e3)
-    bm = byte_model(N, E, K, H)
+    bm = byte_model(N, E, K, H, fp8=fp8, delivered=delivered)
     peak, peak_kind = measured_peaks()
     mean = {k: statistics.fmean(v) for k, v in stage.items()}
     kernels = {}
@@ -343,7 +363,8 @@ def run_ours(args, world, rank, local):
     dc_per = dc_ms / steps
     comb_gbs = bm["combine"] / (mean["combine"] / 1e3) / 1e9
     # the committed counters describe the full-size launch only
-    traffic = None if args.tokens_per_rank else ncu_traffic("combine", ["combine.cu"])
+    full = not args.tokens_per_rank and args.workload == "prefill"
+    traffic = ncu_traffic("combine", ["combine.cu"]) if full else None
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -357,14 +378,18 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC if not args.tokens_per_rank else
-                   f"prefill shape at 8 ranks x {args.tokens_per_rank} tokens",
+        "config": {"workload": WORKLOAD_DESC if full else
+                   f"{args.workload}: {describe_workload(w, N)}",
                    "R": w.R, "N": N, "E": E, "K": K, "H": H,
-                   "layout": "contiguous", "dispatch_dtype": "fp8_e4m3_1x128",
+                   "layout": "contiguous" if layout == ep.EP_LAYOUT_CONTIG else
+                   f"masked, capacity {cap}",
+                   "dispatch_dtype": "fp8_e4m3_1x128" if fp8 else "bf16",
+                   "rows_delivered": delivered,
+                   "expert_renumbering": bool(w.relabel),
                    "step": ("route+layout (one fused kernel)" if fused else
                             "route, layout") + ", dispatch, combine",
-                   "l2": "flushed between steps (512 MiB write, outside the step events); "
-                         "inputs (x 0.47 GB, y 3.76 GB) also exceed L2",
+                   "l2": "flushed between steps (512 MiB write, outside the step events)" +
+                         ("; inputs (x 0.47 GB, y 3.76 GB) also exceed L2" if full else ""),
                    "parallelism": f"{world} independent replica(s), one per GPU"},
         "roofline": {"kernel": "combine", "bound": "hbm", "achieved": round(comb_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(comb_gbs / peak, 4),
@@ -525,13 +550,16 @@ def decode_latency(args, ep, torch, dev, stream, flush):
 
 # ------------------------------------------------------------- CPU oracle --
 
-def oracle_sample(tokens_per_rank: int, seed: int):
-    """The prefill workload's recipe at a bounded size: 8 ranks x
-    tokens_per_rank tokens, same E/K/H, distributions and dtypes."""
+def oracle_sample(workload: str, tokens_per_rank: int, seed: int):
+    """The workload's recipe at a bounded size: its R ranks x tokens_per_rank
+    tokens (0: the workload's own batch sizes), same E/K/H, distributions,
+    layout and dtypes."""
     import numpy as np
     import torch
     from combine_ep_route_topk_gb300 import workloads as wl
-    w = wl.WORKLOADS["prefill"].scaled(batch=("fixed", tokens_per_rank))
+    w = wl.WORKLOADS[workload]
+    if tokens_per_rank:
+        w = w.scaled(batch=("fixed", tokens_per_rank))
     inp = wl.make_inputs(w, seed=seed)
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
     return w, dict(logits=inp["logits"].numpy(), ro=inp["rank_offsets"].numpy(),
@@ -539,19 +567,28 @@ def oracle_sample(tokens_per_rank: int, seed: int):
 
 
 def oracle_step(w, s):
+    """The oracle's whole path for one sample: route (with the balanced
+    renumbering measured on the sample when the workload uses it), layout,
+    dispatch, combine."""
     import oracle
-    idx, wt = oracle.route_topk(s["logits"], w.K)
-    lay = oracle.layout(idx, s["ro"], w.E)
-    oracle.dispatch(s["x"], idx, lay["pos"], lay["expert_offsets"], w.E,
-                    layout=oracle.LAYOUT_CONTIG, dtype=oracle.DTYPE_FP8)
-    oracle.combine(s["y"], idx, wt, lay["pos"], lay["expert_offsets"], w.E)
+    cap = w.cap if w.layout == oracle.LAYOUT_MASKED else 0
+    emap = None
+    if w.relabel:
+        i0, _ = oracle.route_topk(s["logits"], w.K)
+        emap = oracle.balance_map(oracle.layout(i0, s["ro"], w.E)["counts"])
+    idx, wt = oracle.route_topk(s["logits"], w.K, expert_map=emap)
+    lay = oracle.layout(idx, s["ro"], w.E, cap)
+    oracle.dispatch(s["x"], idx, lay["pos"], lay["expert_offsets"], w.E, layout=w.layout,
+                    cap=cap, dtype=w.dtype)
+    oracle.combine(s["y"], idx, wt, lay["pos"], lay["expert_offsets"], w.E, layout=w.layout,
+                   cap=cap)
 
 
 def cpu_baseline(budget_s: float = 12.0):
     """The oracle as it stands, one thread, on sub-batches of the prefill
     workload (8 ranks x 256 tokens each) until about budget_s of CPU work."""
     per_rank = 256
-    w, s = oracle_sample(per_rank, seed=1000)
+    w, s = oracle_sample("prefill", per_rank, seed=1000)
     total_tok, total_s, reps = 0, 0.0, 0
     while total_s < budget_s and reps < 64:
         t0 = time.perf_counter()
@@ -569,11 +606,21 @@ def cpu_baseline(budget_s: float = 12.0):
 def run_reference(args, world, rank):
     if rank != 0:
         return None
-    # bounded per-step sample so warm-up + steps take about 90 s of CPU
-    per_token_s = 0.6e-3
-    per_rank = int(90.0 / (per_token_s * max(1, args.steps + args.warmup)) / 8)
-    per_rank = max(4, min(512, per_rank))
-    w, s = oracle_sample(per_rank, seed=args.seed)
+    from combine_ep_route_topk_gb300 import workloads as wl
+    w0 = wl.WORKLOADS[args.workload]
+    # per-token cost from a small calibration sample, then a per-step sample
+    # sized so warm-up + steps take about 90 s of CPU
+    wc, sc = oracle_sample(args.workload, 8, seed=args.seed)
+    t0 = time.perf_counter()
+    oracle_step(wc, sc)
+    per_token_s = max(1e-7, (time.perf_counter() - t0) / sc["N"])
+    per_rank = int(90.0 / (per_token_s * max(1, args.steps + args.warmup)) / w0.R)
+    full = wl.make_inputs(w0, seed=args.seed, with_y=False)["N"] // w0.R
+    if per_rank >= full:
+        per_rank = 0  # the workload's own batch fits the budget
+    else:
+        per_rank = max(4, per_rank)
+    w, s = oracle_sample(args.workload, per_rank, seed=args.seed)
     for _ in range(args.warmup):
         oracle_step(w, s)
     times = []
@@ -583,16 +630,19 @@ def run_reference(args, world, rank):
         times.append(time.perf_counter() - t0)
     tot = sum(times)
     value = s["N"] * args.steps / tot
+    sample = (f"each step: the whole batch ({s['N']} tokens)" if not per_rank else
+              f"each step: {w.R} ranks x {per_rank} tokens ({s['N']} tokens) of the workload")
+    desc = WORKLOAD_DESC if args.workload == "prefill" else \
+        f"{args.workload}: {describe_workload(w0, full * w0.R)}"
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC, "step": "route+layout+dispatch+combine",
-                   "sample_per_step": f"8 ranks x {per_rank} tokens of the same workload"},
+        "config": {"workload": desc, "step": "route+layout+dispatch+combine",
+                   "sample_per_step": sample},
         "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
-                         "kind": "oracle",
-                         "sample": f"each step: 8 ranks x {per_rank} tokens ({s['N']} tokens)"},
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -609,6 +659,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--fused", action="store_true",
                     help="route + layout as the one cooperative kernel (ep_route_layout)")
+    ap.add_argument("--workload", default="prefill",
+                    choices=["toy", "lumpy", "decode", "prefill", "skew"],
+                    help="the workload a step runs (default: prefill, the headline)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the overlap, chunked and decode measurements (profiling)")
     ap.add_argument("--decode-only", action="store_true",
