@@ -7,8 +7,8 @@
 //
 // fp32 accumulation, one fused multiply-add per pick in pick order (so the
 // result is reproducible bit for bit), undelivered picks skipped.  One block
-// per token; each thread owns 16-byte column vectors and issues the loads of
-// all K rows before the FMAs (K templated for 1/2/4/8, so up to 8 x 16 B per
+// per token (256 threads, picked by a block-size sweep); each thread owns
+// 16-byte column vectors and issues the loads of all K rows before the FMAs (K templated for 1/2/4/8, so up to 8 x 16 B per
 // vector are in flight per thread).  Bytes per token: K*H*2 read + H*2
 // written; HBM-bound.
 #include <cuda_bf16.h>
@@ -93,11 +93,11 @@ cudaError_t launch_combine(const MoveArgs& a, cudaStream_t s) {
     if (a.N == 0) return cudaSuccess;
     cudaError_t err;
     switch (a.K) {
-        case 1: err = launch(combine_kernel<128, 1>, dim3(a.N), dim3(128), 0, s, a); break;
-        case 2: err = launch(combine_kernel<128, 2>, dim3(a.N), dim3(128), 0, s, a); break;
-        case 4: err = launch(combine_kernel<128, 4>, dim3(a.N), dim3(128), 0, s, a); break;
-        case 8: err = launch(combine_kernel<128, 8>, dim3(a.N), dim3(128), 0, s, a); break;
-        default: err = launch(combine_kernel<128, 0>, dim3(a.N), dim3(128), 0, s, a); break;
+        case 1: err = launch(combine_kernel<256, 1>, dim3(a.N), dim3(256), 0, s, a); break;
+        case 2: err = launch(combine_kernel<256, 2>, dim3(a.N), dim3(256), 0, s, a); break;
+        case 4: err = launch(combine_kernel<256, 4>, dim3(a.N), dim3(256), 0, s, a); break;
+        case 8: err = launch(combine_kernel<256, 8>, dim3(a.N), dim3(256), 0, s, a); break;
+        default: err = launch(combine_kernel<256, 0>, dim3(a.N), dim3(256), 0, s, a); break;
     }
     note_launch();
     return err;
