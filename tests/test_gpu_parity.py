@@ -54,8 +54,9 @@ def test_worked_example_on_gpu():
     np.testing.assert_allclose(np_(w), ref_w, rtol=weight_rtol())
 
 
-@pytest.mark.parametrize("E,K", [(16, 2), (16, 16), (100, 7), (128, 4), (256, 8), (384, 8),
-                                 (512, 32), (1024, 8), (33, 1), (1, 1)])
+@pytest.mark.parametrize("E,K", [(16, 2), (16, 16), (100, 7), (128, 4), (128, 8), (256, 4),
+                                 (256, 8), (256, 2), (384, 8), (512, 32), (1024, 8), (33, 1),
+                                 (1, 1)])
 def test_route_topk_random(E, K):
     g = torch.Generator().manual_seed(E * 7 + K)
     N = 777  # ragged against the 8-token blocks
@@ -66,7 +67,7 @@ def test_route_topk_random(E, K):
     np.testing.assert_allclose(np_(w), ref_w, rtol=weight_rtol())
 
 
-@pytest.mark.parametrize("E,K", [(16, 2), (256, 8), (100, 5)])
+@pytest.mark.parametrize("E,K", [(16, 2), (128, 4), (256, 8), (100, 5)])
 def test_route_topk_ties_and_signed_zero(E, K):
     rng = np.random.default_rng(E + K)
     vals = rng.choice(np.array([-1.0, -0.0, 0.0, 0.25, 1.0], np.float32), size=(300, E))
@@ -82,6 +83,17 @@ def test_route_topk_expert_map():
     emap = torch.randperm(128, generator=g).to(torch.int32)
     idx, w = ep_route_topk(logits.cuda(), 4, expert_map=emap.cuda())
     ref_idx, ref_w = oracle.route_topk(logits.numpy(), 4, expert_map=emap.numpy())
+    np.testing.assert_array_equal(np_(idx), ref_idx)
+    np.testing.assert_allclose(np_(w), ref_w, rtol=weight_rtol())
+
+
+@pytest.mark.parametrize("N", [1, 2, 15, 17])
+def test_route_topk_few_tokens(N):
+    """Fewer tokens than one block serves (one or two tokens per warp)."""
+    g = torch.Generator().manual_seed(N)
+    logits = torch.randn(N, 256, generator=g)
+    idx, w = ep_route_topk(logits.cuda(), 8)
+    ref_idx, ref_w = oracle.route_topk(logits.numpy(), 8)
     np.testing.assert_array_equal(np_(idx), ref_idx)
     np.testing.assert_allclose(np_(w), ref_w, rtol=weight_rtol())
 
