@@ -111,3 +111,109 @@ def test_chunked_identity_experts_return_x():
                lambda t0, n, out, sc, lay: out, comb)
     torch.cuda.synchronize()
     assert torch.equal(comb.view(torch.int16), x.view(torch.int16))
+
+
+def _pinned(t):
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h.copy_(t)
+    return h
+
+
+@pytest.mark.parametrize("name,dtype", [("lumpy", ep.EP_DTYPE_BF16),
+                                        ("prefill", ep.EP_DTYPE_FP8_E4M3_B128)])
+def test_host_pipeline_matches_single_batch(name, dtype):
+    """Steps over pinned host buffers, copies overlapped across steps: every
+    step's result and the last step's dispatched rows equal the single-batch
+    path's on the same inputs, bit for bit (including a reused buffer set)."""
+    w = wl.WORKLOADS[name]
+    if name == "prefill":
+        w = w.scaled(batch=("uniform", 200, 300))
+    E, K, H = w.E, w.K, w.H
+    cases = []
+    for seed in (21, 22):
+        inp = wl.make_inputs(w, seed=seed, with_y=False)
+        N = inp["N"]
+        idx, wt = ep.ep_route_topk(inp["logits"].cuda(), K)
+        lay = ep.ep_dispatch_layout(idx, inp["rank_offsets"].cuda(), E)
+        out, sc = ep.ep_dispatch(inp["x"].cuda(), idx, lay.pos, lay.expert_offsets, E,
+                                 ep.EP_LAYOUT_CONTIG, 0, dtype)
+        y = _scaled(out, sc, lay, E, N * K)
+        comb = ep.ep_combine(y, idx, wt, lay.pos, lay.expert_offsets, E)
+        cases.append(dict(N=N, x=_pinned(inp["x"]), logits=_pinned(inp["logits"]),
+                          ro=_pinned(inp["rank_offsets"]), y=_pinned(y.cpu()),
+                          comb=comb.cpu(), out=out.cpu(), sc=None if sc is None else sc.cpu()))
+    # the seeds draw different batch sizes, so each gets its own pipeline
+    for c in cases:
+        hp = pl.HostPipeline(c["N"], E, K, H, w.R, dtype)
+        outs = [torch.empty(c["N"], H, dtype=torch.bfloat16, pin_memory=True) for _ in range(3)]
+        for o in outs:
+            hp.step(c["x"], c["logits"], c["ro"], c["y"], o)
+        hp.synchronize()
+        for o in outs:
+            assert torch.equal(o, c["comb"])
+        assert torch.equal(hp.out.cpu(), c["out"])
+        if c["sc"] is not None:
+            assert torch.equal(hp.scales.cpu(), c["sc"])
+
+
+def test_host_pipeline_alternating_inputs():
+    """Alternating two input sets of one size through a depth-2 pipeline: each
+    step's result is its own inputs' (no buffer set is overwritten early)."""
+    w = wl.WORKLOADS["lumpy"]
+    E, K, H = w.E, w.K, w.H
+    g = torch.Generator().manual_seed(3)
+    N, R = 700, 4
+    ro = torch.tensor([0, 100, 350, 351, 700], dtype=torch.int32)
+    sets = []
+    for _ in range(2):
+        logits = torch.randn(N, E, generator=g)
+        x = torch.randn(N, H, generator=g).to(torch.bfloat16)
+        y = torch.randn(N * K, H, generator=g).to(torch.bfloat16)
+        idx, wt = ep.ep_route_topk(logits.cuda(), K)
+        lay = ep.ep_dispatch_layout(idx, ro.cuda(), E)
+        comb = ep.ep_combine(y.cuda(), idx, wt, lay.pos, lay.expert_offsets, E)
+        sets.append((_pinned(x), _pinned(logits), _pinned(ro), _pinned(y), comb.cpu()))
+    hp = pl.HostPipeline(N, E, K, H, R, ep.EP_DTYPE_BF16)
+    order = [0, 1, 0, 1, 1, 0]
+    outs = [torch.empty(N, H, dtype=torch.bfloat16, pin_memory=True) for _ in order]
+    for i, o in zip(order, outs):
+        x, lg, r, y, _ = sets[i]
+        hp.step(x, lg, r, y, o)
+    hp.synchronize()
+    for i, o in zip(order, outs):
+        assert torch.equal(o, sets[i][4])
+
+
+def test_host_pipeline_masked_with_expert_map():
+    """The decode shape (masked capacity, overflow dropped) with a balanced
+    renumbering map: each step's result equals the single-batch path's."""
+    w = wl.WORKLOADS["decode"].scaled(batch=("uniform", 20, 60))
+    E, K, H, cap = w.E, w.K, w.H, 4  # small capacity: some picks overflow
+    inp = wl.make_inputs(w, seed=9, with_y=False)
+    N = inp["N"]
+    logits, ro, x = inp["logits"].cuda(), inp["rank_offsets"].cuda(), inp["x"].cuda()
+    i0, _ = ep.ep_route_topk(logits, K)
+    emap = ep.ep_expert_balance_map(ep.ep_dispatch_layout(i0, ro, E).counts)
+    idx, wt = ep.ep_route_topk(logits, K, expert_map=emap)
+    lay = ep.ep_dispatch_layout(idx, ro, E, cap)
+    assert int(lay.overflow_count.item()) > 0
+    g = torch.Generator().manual_seed(4)
+    y = torch.randn(E, cap, H, generator=g).to(torch.bfloat16)
+    comb = ep.ep_combine(y.cuda(), idx, wt, lay.pos, lay.expert_offsets, E,
+                         ep.EP_LAYOUT_MASKED, cap).cpu()
+    out, _ = ep.ep_dispatch(x, idx, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_MASKED, cap,
+                            ep.EP_DTYPE_BF16)
+    hp = pl.HostPipeline(N, E, K, H, w.R, ep.EP_DTYPE_BF16, cap=cap, expert_map=emap)
+    outs = [torch.empty(N, H, dtype=torch.bfloat16, pin_memory=True) for _ in range(3)]
+    args = [_pinned(t) for t in (inp["x"], inp["logits"], inp["rank_offsets"], y)]
+    for o in outs:
+        hp.step(*args, o)
+    hp.synchronize()
+    for o in outs:
+        assert torch.equal(o, comb)
+    # only the delivered slots of the masked buffer are defined
+    m = hp.layout.masked_m.cpu()
+    ref = out.cpu().view(E, cap, H)
+    got = hp.out.cpu().view(E, cap, H)
+    for e in range(E):
+        assert torch.equal(got[e, :m[e]], ref[e, :m[e]])
