@@ -15,7 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libep_gb300.so")
-SOURCES = ["ep_api.cu", "route_topk.cu", "layout.cu", "layout_static.cu", "route_layout.cu",
+SOURCES = ["ep_api.cu", "route_topk.cu", "layout.cu", "layout_cluster.cu", "layout_static.cu",
+           "route_layout.cu",
            "dispatch.cu", "combine.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ep_kernels.cuh", "route_common.cuh",
                                             "layout_common.cuh")] + [

@@ -81,6 +81,9 @@ struct LayoutArgs {
     int32_t* ws_totals;  // [E] expert totals
 };
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t s);
+// Small problems: the whole layout in one thread-block cluster (no workspace).
+bool layout_cluster_fits(int N, int E, int K, int R);
+cudaError_t launch_layout_cluster(const LayoutArgs& a, cudaStream_t s);
 
 // ---- fused route + layout (one cooperative kernel) ------------------------
 int route_layout_chunk_tokens(int N);

@@ -16,7 +16,8 @@
 //              per-warp bases and __match_any_sync ranks, so the result never
 //              depends on atomic ordering.
 // Everything stays on the device (no host read of a count), so the masked
-// decode path can be captured in a CUDA graph.
+// decode path can be captured in a CUDA graph.  Problems small enough for one
+// thread-block cluster take the one-launch variant in layout_cluster.cu.
 #include "layout_common.cuh"
 
 namespace ep {
@@ -145,6 +146,10 @@ __global__ void __launch_bounds__(kNT) layout_scatter_kernel(LayoutArgs a, int C
 }  // namespace
 
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t s) {
+    if (layout_cluster_fits(a.N, a.E, a.K, a.R)) {  // layout_cluster.cu
+        note_launch(1);
+        return launch_layout_cluster(a, s);
+    }
     const int C = layout_chunk_tokens(a.N);
     const int slots = layout_chunk_slots(a.N, a.R);
     const int tab = 2 * ((a.R + 1 + 3) & ~3) + 32;

@@ -113,7 +113,7 @@ __device__ __forceinline__ int chunk_rank(const int* s_tab, int R, int c) {
     return lo;
 }
 
-__device__ __forceinline__ int round_up4(int v) { return (v + 3) & ~3; }
+__host__ __device__ __forceinline__ int round_up4(int v) { return (v + 3) & ~3; }
 
 
 // Expert offsets: s_eoff[0..E] = exclusive prefix of totals[0..E-1].

@@ -106,10 +106,22 @@ def test_route_topk_empty_batch():
 
 # ----------------------------------------------------------------- layout ---
 
+@pytest.fixture(params=["cluster", "kernels"])
+def layout_path(request, monkeypatch):
+    """The layout's two implementations: one thread-block cluster (problems up
+    to 32768 picks whose chunk rows fit in shared memory) and the three
+    kernels (every size; forced with EP_LAYOUT_CLUSTER=0)."""
+    if request.param == "kernels":
+        monkeypatch.setenv("EP_LAYOUT_CLUSTER", "0")
+    else:
+        monkeypatch.delenv("EP_LAYOUT_CLUSTER", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("name,seed", [("toy", 0), ("lumpy", 0), ("lumpy", 1), ("lumpy", 2),
                                        ("lumpy", 3), ("lumpy", 4), ("decode", 0), ("prefill", 0),
                                        ("skew", 0)])
-def test_layout_parity(name, seed):
+def test_layout_parity(name, seed, layout_path):
     w = _small(name)
     inp = wl.make_inputs(w, seed=seed, with_y=False)
     idx, _ = oracle.route_topk(inp["logits"].numpy(), w.K)
@@ -127,8 +139,12 @@ def test_layout_parity(name, seed):
     ([33] * 64, 1024, 32, 2),                    # E = 1024, K = 32, many ranks
     ([1] * 1024, 64, 4, 100),                    # R = 1024
     ([5000, 1, 3000], 256, 8, 64),               # chunks > 32 tokens, ragged
+    ([125] * 8, 1024, 8, 16),                    # E = 1024: 140 KB of chunk rows per CTA
+    ([128] * 8, 1024, 32, 40),                   # 32768 picks: the largest one-cluster case
+    ([4096, 1], 16, 8, 2000),                    # just over it: the three kernels
+    ([1] * 1024, 16, 2, 1),                      # R = 1024 with one-token ranks
 ])
-def test_layout_edge_cases(B, E, K, cap):
+def test_layout_edge_cases(B, E, K, cap, layout_path):
     g = torch.Generator().manual_seed(len(B) * E + K)
     N = sum(B)
     offs = np.concatenate([[0], np.cumsum(B)]).astype(np.int32)
@@ -139,7 +155,7 @@ def test_layout_edge_cases(B, E, K, cap):
     _check_layout(gpu, ref, cap)
 
 
-def test_layout_all_tokens_one_expert_and_invalid_ids():
+def test_layout_all_tokens_one_expert_and_invalid_ids(layout_path):
     N, E, K = 300, 16, 2
     idx = np.zeros((N, K), np.int32)
     idx[:, 1] = np.arange(N) % E
@@ -151,6 +167,29 @@ def test_layout_all_tokens_one_expert_and_invalid_ids():
     assert ref["overflow"] > 0
     gpu = ep_dispatch_layout(torch.from_numpy(idx).cuda(), torch.from_numpy(offs).cuda(), E, cap)
     _check_layout(gpu, ref, cap)
+
+
+@pytest.mark.parametrize("B,E,K,expect", [
+    ([128] * 8, 256, 8, 1),        # the decode shape: one cluster
+    ([128] * 8, 1024, 32, 1),      # 32768 picks
+    ([4096, 1], 16, 8, 3),         # 32776 picks: three kernels
+    ([4096] * 8, 256, 8, 3),       # the prefill shape
+])
+def test_layout_path_choice(B, E, K, expect, monkeypatch):
+    """Which implementation serves a size (launches per layout call)."""
+    from combine_ep_route_topk_gb300 import ep as epb
+    monkeypatch.delenv("EP_LAYOUT_CLUSTER", raising=False)
+    N = sum(B)
+    offs = torch.tensor(np.concatenate([[0], np.cumsum(B)]), dtype=torch.int32, device="cuda")
+    idx = torch.zeros(N, K, dtype=torch.int32, device="cuda")
+    before = epb.lib().ep_kernel_launch_count()
+    ep_dispatch_layout(idx, offs, E)
+    assert epb.lib().ep_kernel_launch_count() - before == expect
+    monkeypatch.setenv("EP_LAYOUT_CLUSTER", "0")
+    before = epb.lib().ep_kernel_launch_count()
+    ep_dispatch_layout(idx, offs, E)
+    assert epb.lib().ep_kernel_launch_count() - before == 3
+    torch.cuda.synchronize()
 
 
 # --------------------------------------------------------------- dispatch ---
@@ -254,6 +293,29 @@ def test_combine_masked_with_overflow_and_runtime_k():
     y = torch.randn(w.E * cap, w.H, generator=g).to(torch.bfloat16)
     got, ref = _combine_both(y, idx, wts, lay, w.E, EP_LAYOUT_MASKED, cap)
     assert combine_rel_err(got, ref) <= COMBINE_RTOL
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("H,dtype", [(8, EP_DTYPE_BF16), (136, EP_DTYPE_BF16),
+                                     (16392, EP_DTYPE_BF16), (128, EP_DTYPE_FP8_E4M3_B128),
+                                     (16512, EP_DTYPE_FP8_E4M3_B128)])
+@pytest.mark.parametrize("layout", [EP_LAYOUT_CONTIG, EP_LAYOUT_MASKED])
+def test_dispatch_combine_hidden_sizes(H, dtype, layout):
+    """Smallest rows (one 16-byte vector, one scale block) and rows longer
+    than one pass of a block (several column passes with a ragged last one,
+    in dispatch and in combine)."""
+    g = torch.Generator().manual_seed(H + layout)
+    B, E, K = [9, 0, 28], 16, 3
+    N = sum(B)
+    offs = np.concatenate([[0], np.cumsum(B)]).astype(np.int32)
+    idx, wts = oracle.route_topk(torch.randn(N, E, generator=g).numpy(), K)
+    cap = 5 if layout == EP_LAYOUT_MASKED else 0
+    lay = oracle.layout(idx, offs, E, cap)
+    x = (torch.randn(N, H, generator=g) * 3).to(torch.bfloat16)
+    _dispatch_both(x, idx, lay, E, layout, cap, dtype)
+    rows = N * K if layout == EP_LAYOUT_CONTIG else E * cap
+    y = torch.randn(rows, H, generator=g).to(torch.bfloat16)
+    got, ref = _combine_both(y, idx, wts, lay, E, layout, cap)
     np.testing.assert_array_equal(got, ref)
 
 
