@@ -36,9 +36,20 @@ using namespace lay;
 constexpr int kCS = 8;         // CTAs of the cluster (portable cluster size)
 constexpr int kCT = 512;       // threads of a CTA
 constexpr int kCW = kCT / 32;  // warps of a CTA
-constexpr int kU = 4;          // 32-pick passes whose loads are issued together
+#ifndef EP_LAYOUT_CLUSTER_U
+#define EP_LAYOUT_CLUSTER_U 4
+#endif
+#ifndef EP_LAYOUT_CLUSTER_MAX_PICKS
+#define EP_LAYOUT_CLUSTER_MAX_PICKS (1 << 14)
+#endif
+constexpr int kU = EP_LAYOUT_CLUSTER_U;  // 32-pick passes whose loads are issued together
 constexpr size_t kMaxSmem = 160 * 1024;
-constexpr long long kMaxPicks = 1 << 15;
+// Larger problems take the three kernels: measured on GB300 (E = 256, K = 8,
+// 8 ranks), the cluster takes 13.0 / 15.0 / 21.2 us at 8192 / 16384 / 32768
+// picks against 15.1 / 17.1 / 18.0 us; at 64 ranks and 32768 picks, 31.4
+// against 20.1 us.
+constexpr long long kMaxPicks = EP_LAYOUT_CLUSTER_MAX_PICKS;
+constexpr int kMaxRanks = 64;
 
 struct ClusterPlan {
     int C;        // tokens per chunk
@@ -268,13 +279,13 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kCT)
 
 }  // namespace
 
-// The one-cluster path serves problems of at most kMaxPicks picks whose
-// chunk rows fit in shared memory.  EP_LAYOUT_CLUSTER=0 in the environment
+// The one-cluster path serves problems of at most kMaxPicks picks and
+// kMaxRanks ranks whose chunk rows fit in shared memory.  EP_LAYOUT_CLUSTER=0 in the environment
 // (read at every call) selects the three-kernel path for every size.
 bool layout_cluster_fits(int N, int E, int K, int R) {
     const char* v = std::getenv("EP_LAYOUT_CLUSTER");
     if (v && v[0] == '0') return false;
-    if ((long long)N * K > kMaxPicks) return false;
+    if ((long long)N * K > kMaxPicks || R > kMaxRanks) return false;
     return cluster_plan(N, E, R).smem <= kMaxSmem;
 }
 

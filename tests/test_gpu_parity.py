@@ -109,8 +109,8 @@ def test_route_topk_empty_batch():
 @pytest.fixture(params=["cluster", "kernels"])
 def layout_path(request, monkeypatch):
     """The layout's two implementations: one thread-block cluster (problems up
-    to 32768 picks whose chunk rows fit in shared memory) and the three
-    kernels (every size; forced with EP_LAYOUT_CLUSTER=0)."""
+    to 16384 picks and 64 ranks whose chunk rows fit in shared memory) and
+    the three kernels (every size; forced with EP_LAYOUT_CLUSTER=0)."""
     if request.param == "kernels":
         monkeypatch.setenv("EP_LAYOUT_CLUSTER", "0")
     else:
@@ -139,9 +139,11 @@ def test_layout_parity(name, seed, layout_path):
     ([33] * 64, 1024, 32, 2),                    # E = 1024, K = 32, many ranks
     ([1] * 1024, 64, 4, 100),                    # R = 1024
     ([5000, 1, 3000], 256, 8, 64),               # chunks > 32 tokens, ragged
-    ([125] * 8, 1024, 8, 16),                    # E = 1024: 140 KB of chunk rows per CTA
-    ([128] * 8, 1024, 32, 40),                   # 32768 picks: the largest one-cluster case
-    ([4096, 1], 16, 8, 2000),                    # just over it: the three kernels
+    ([125] * 8, 1024, 8, 16),                    # E = 1024: 90 KB of shared memory per CTA
+    ([64] * 8, 1024, 32, 40),                    # 16384 picks: the largest one-cluster case
+    ([2048, 1], 16, 8, 2000),                    # just over it: the three kernels
+    ([16] * 64, 64, 4, 3),                       # 64 ranks: the widest one-cluster chunk table
+    ([0, 3] * 32 + [5], 32, 2, 1),               # 65 ranks, empty ones: the three kernels
     ([1] * 1024, 16, 2, 1),                      # R = 1024 with one-token ranks
 ])
 def test_layout_edge_cases(B, E, K, cap, layout_path):
@@ -171,8 +173,10 @@ def test_layout_all_tokens_one_expert_and_invalid_ids(layout_path):
 
 @pytest.mark.parametrize("B,E,K,expect", [
     ([128] * 8, 256, 8, 1),        # the decode shape: one cluster
-    ([128] * 8, 1024, 32, 1),      # 32768 picks
-    ([4096, 1], 16, 8, 3),         # 32776 picks: three kernels
+    ([64] * 8, 1024, 32, 1),       # 16384 picks
+    ([2048, 1], 16, 8, 3),         # 16392 picks: three kernels
+    ([16] * 64, 64, 4, 1),         # 64 ranks
+    ([16] * 65, 65, 4, 3),         # 65 ranks: three kernels
     ([4096] * 8, 256, 8, 3),       # the prefill shape
 ])
 def test_layout_path_choice(B, E, K, expect, monkeypatch):
