@@ -487,25 +487,32 @@ def two_batch_overlap(args, ep, torch, dev, main_stream, inp, w, flush, dist):
 
 def chunked_prefill(args, ep, torch, dev, main_stream, inp, w, flush, dist, T=8192):
     """The same batch in ant-moving rounds of T tokens (pipeline.chunked): the
-    dispatch buffer holds T*K rows instead of N*K."""
+    dispatch buffer holds T*K rows instead of N*K.  Rounds in order with one
+    buffer set, and alternating over two sets (and streams)."""
     from combine_ep_route_topk_gb300 import pipeline as pl
     K, H, E, R = w.K, w.H, w.E, w.R
     comb = torch.empty(inp["N"], H, dtype=torch.bfloat16, device=dev)
-    bufs = pl.make_chunk_buffers(T, E, K, H, R, ep.EP_DTYPE_FP8_E4M3_B128, dev)
     offs = inp["rank_offsets"].cpu().tolist()
     ro_rounds = pl.chunk_rank_offsets(offs, inp["N"], T, dev)
     y = inp["y"]
+    out = {}
+    for sets in (1, 2):
+        bufs = pl.make_chunk_buffers(T, E, K, H, R, ep.EP_DTYPE_FP8_E4M3_B128, dev, sets=sets)
 
-    def step():
-        pl.chunked(inp["logits"], inp["x"], offs, K, ep.EP_DTYPE_FP8_E4M3_B128, bufs,
-                   lambda t0, n, out, sc, lay: y[t0 * K:(t0 + n) * K], comb,
-                   ro_rounds=ro_rounds)
+        def step():
+            pl.chunked(inp["logits"], inp["x"], offs, K, ep.EP_DTYPE_FP8_E4M3_B128, bufs,
+                       lambda t0, n, o, sc, lay: y[t0 * K:(t0 + n) * K], comb,
+                       ro_rounds=ro_rounds)
 
-    res = _time_schedule(args, torch, main_stream, flush, dist, step, inp["N"],
-                         f"rounds of {T} tokens")
-    res["dispatch_buffer_bytes"] = bufs.dispatch_bytes
-    res["dispatch_buffer_bytes_unchunked"] = inp["N"] * K * (H + H // 128 * 4)
-    return res
+        res = _time_schedule(args, torch, main_stream, flush, dist, step, inp["N"],
+                             f"rounds of {T} tokens, {sets} buffer set(s)" +
+                             (" on alternating streams" if sets > 1 else ""))
+        res["dispatch_buffer_bytes"] = sum(b.dispatch_bytes for b in
+                                           (bufs if sets > 1 else [bufs]))
+        res["dispatch_buffer_bytes_unchunked"] = inp["N"] * K * (H + H // 128 * 4)
+        out["in_order" if sets == 1 else "alternating_2_sets"] = res
+        del bufs
+    return out
 
 
 def _time_schedule(args, torch, main_stream, flush, dist, step, N, note):

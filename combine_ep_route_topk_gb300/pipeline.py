@@ -15,7 +15,10 @@ chunked
     so the dispatch buffer is bounded by round_tokens * K rows instead of
     N * K.  Each round routes, lays out and dispatches its tokens, hands the
     dispatched rows to the caller's expert function, and combines the
-    result into the round's slice of the output.
+    result into the round's slice of the output.  Given two (or more) round
+    buffer sets, rounds alternate over the sets' streams, so one round's
+    latency-bound routing and layout run under the previous round's
+    HBM-bound dispatch and combine.
 
 HostPipeline
     Steps whose inputs and result live in pinned host memory.  Copies in,
@@ -110,13 +113,16 @@ def two_batch_overlap(mbs, K, dtype, expert_out, main_stream=None):
 
 @dataclass
 class ChunkBuffers:
-    """Round-sized buffers: the dispatch buffer holds round_tokens * K rows."""
+    """Round-sized buffers: the dispatch buffer holds round_tokens * K rows.
+    `stream` is the stream of the rounds that use this set when rounds
+    alternate over several sets."""
     round_tokens: int
     idx: torch.Tensor
     wt: torch.Tensor
     ws: torch.Tensor
     out: torch.Tensor
     scales: torch.Tensor | None
+    stream: torch.cuda.Stream | None = None
 
     @property
     def dispatch_bytes(self) -> int:
@@ -126,17 +132,28 @@ class ChunkBuffers:
         return b
 
 
-def make_chunk_buffers(round_tokens, E, K, H, R, dtype, device):
+def make_chunk_buffers(round_tokens, E, K, H, R, dtype, device, sets=1):
+    """One round buffer set (sets == 1), or a list of `sets` sets, each with
+    its own stream, for rounds that alternate over them."""
     fp8 = dtype == _ep.EP_DTYPE_FP8_E4M3_B128
     T = round_tokens
-    return ChunkBuffers(
-        round_tokens=T,
-        idx=torch.empty(T, K, dtype=torch.int32, device=device),
-        wt=torch.empty(T, K, dtype=torch.float32, device=device),
-        ws=torch.empty(_ep.ep_dispatch_layout_workspace_size(T, E, K, R), dtype=torch.uint8,
-                       device=device),
-        out=torch.empty(T * K, H, dtype=torch.uint8 if fp8 else torch.bfloat16, device=device),
-        scales=torch.empty(T * K, H // 128, dtype=torch.float32, device=device) if fp8 else None)
+
+    def one(stream):
+        return ChunkBuffers(
+            round_tokens=T,
+            idx=torch.empty(T, K, dtype=torch.int32, device=device),
+            wt=torch.empty(T, K, dtype=torch.float32, device=device),
+            ws=torch.empty(_ep.ep_dispatch_layout_workspace_size(T, E, K, R), dtype=torch.uint8,
+                           device=device),
+            out=torch.empty(T * K, H, dtype=torch.uint8 if fp8 else torch.bfloat16,
+                            device=device),
+            scales=(torch.empty(T * K, H // 128, dtype=torch.float32, device=device)
+                    if fp8 else None),
+            stream=stream)
+
+    if sets == 1:
+        return one(None)
+    return [one(torch.cuda.Stream(device=device)) for _ in range(sets)]
 
 
 def round_rank_offsets(rank_offsets_host, t0, t1):
@@ -154,35 +171,52 @@ def chunk_rank_offsets(rank_offsets_host, N, T, device):
                                                                       R + 1).to(device)
 
 
-def chunked(logits, x, rank_offsets_host, K, dtype, bufs: ChunkBuffers, expert_out, comb,
-            ro_rounds=None):
-    """Ant-moving rounds over the packed token sequence.  `expert_out(r0, n,
-    out_rows, scales, layout)` returns the bf16 expert outputs [n*K, H] of the
-    round's dispatched rows.  Results land in comb[t0:t1] for each round.
-    `ro_rounds` (chunk_rank_offsets) may be passed to skip the upload.
-    Returns [(t0, t1, layout)] per round (the layouts for inspection)."""
+def chunked(logits, x, rank_offsets_host, K, dtype, bufs, expert_out, comb, ro_rounds=None):
+    """Ant-moving rounds over the packed token sequence.  `bufs` is one
+    ChunkBuffers (rounds in order on the current stream) or a list of them
+    (make_chunk_buffers(..., sets=n)): round j then uses set j mod n on that
+    set's stream, and the current stream waits for every round at the end.
+    `expert_out(t0, n, out_rows, scales, layout)` returns the bf16 expert
+    outputs [n*K, H] of the round's dispatched rows (called on the round's
+    stream).  Results land in comb[t0:t1] for each round.  `ro_rounds`
+    (chunk_rank_offsets) may be passed to skip the upload.  Returns
+    [(t0, t1, layout)] per round (the layouts for inspection)."""
+    sets = list(bufs) if isinstance(bufs, (list, tuple)) else [bufs]
     N, E = logits.shape
-    T = bufs.round_tokens
+    T = sets[0].round_tokens
     starts = list(range(0, N, T))
     # every round's rank offsets in one upload, before the first launch
     ro_all = ro_rounds if ro_rounds is not None else \
         chunk_rank_offsets(rank_offsets_host, N, T, logits.device)
+    main = torch.cuda.current_stream(logits.device)
+    multi = len(sets) > 1
+    if multi:
+        for b in sets:
+            if b.stream is None:
+                raise ValueError("alternating rounds need buffer sets with streams "
+                                 "(make_chunk_buffers(..., sets=n))")
+            b.stream.wait_stream(main)
     rounds = []
     for j, t0 in enumerate(starts):
+        b = sets[j % len(sets)]
         t1 = min(N, t0 + T)
         n = t1 - t0
-        ro = ro_all[j]
-        idx, wt = bufs.idx[:n], bufs.wt[:n]
-        _ep.ep_route_topk(logits[t0:t1], K, topk_idx=idx, topk_w=wt)
-        lay = _ep.ep_dispatch_layout(idx, ro, E, 0, workspace=bufs.ws)
-        out = bufs.out[:n * K]
-        scales = None if bufs.scales is None else bufs.scales[:n * K]
-        _ep.ep_dispatch(x[t0:t1], idx, lay.pos, lay.expert_offsets, E, _ep.EP_LAYOUT_CONTIG, 0,
-                        dtype, out=out, out_scales=scales)
-        y = expert_out(t0, n, out, scales, lay)
-        _ep.ep_combine(y, idx, wt, lay.pos, lay.expert_offsets, E, _ep.EP_LAYOUT_CONTIG, 0,
-                       out=comb[t0:t1])
+        with torch.cuda.stream(b.stream if multi else main):
+            ro = ro_all[j]
+            idx, wt = b.idx[:n], b.wt[:n]
+            _ep.ep_route_topk(logits[t0:t1], K, topk_idx=idx, topk_w=wt)
+            lay = _ep.ep_dispatch_layout(idx, ro, E, 0, workspace=b.ws)
+            out = b.out[:n * K]
+            scales = None if b.scales is None else b.scales[:n * K]
+            _ep.ep_dispatch(x[t0:t1], idx, lay.pos, lay.expert_offsets, E, _ep.EP_LAYOUT_CONTIG,
+                            0, dtype, out=out, out_scales=scales)
+            y = expert_out(t0, n, out, scales, lay)
+            _ep.ep_combine(y, idx, wt, lay.pos, lay.expert_offsets, E, _ep.EP_LAYOUT_CONTIG, 0,
+                           out=comb[t0:t1])
         rounds.append((t0, t1, lay))
+    if multi:
+        for b in sets:
+            main.wait_stream(b.stream)
     return rounds
 
 

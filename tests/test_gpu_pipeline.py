@@ -74,7 +74,8 @@ def test_two_batch_overlap_matches_single_batch(name, dtype):
 @pytest.mark.parametrize("name,dtype,T", [("lumpy", ep.EP_DTYPE_BF16, 300),
                                           ("skew", ep.EP_DTYPE_BF16, 4096),
                                           ("prefill", ep.EP_DTYPE_FP8_E4M3_B128, 640)])
-def test_chunked_rounds_match_single_batch(name, dtype, T):
+@pytest.mark.parametrize("sets", [1, 2, 3])
+def test_chunked_rounds_match_single_batch(name, dtype, T, sets):
     w = wl.WORKLOADS[name]
     if name == "prefill":
         w = w.scaled(batch=("uniform", 200, 300))
@@ -83,12 +84,13 @@ def test_chunked_rounds_match_single_batch(name, dtype, T):
     offs = inp["rank_offsets"].tolist()
     logits, x = inp["logits"].cuda(), inp["x"].cuda()
     comb = torch.empty(N, H, dtype=torch.bfloat16, device="cuda")
-    bufs = pl.make_chunk_buffers(T, E, K, H, R, dtype, "cuda")
+    bufs = pl.make_chunk_buffers(T, E, K, H, R, dtype, "cuda", sets=sets)
     rounds = pl.chunked(logits, x, offs, K, dtype, bufs,
                         lambda t0, n, out, sc, lay: _scaled(out, sc, lay, E, n * K), comb)
     torch.cuda.synchronize()
     assert len(rounds) == (N + T - 1) // T > 1
-    assert bufs.out.shape[0] == T * K  # the dispatch buffer is bounded by the round
+    for b in (bufs if sets > 1 else [bufs]):
+        assert b.out.shape[0] == T * K  # each dispatch buffer is bounded by the round
     ref = _single_batch(inp, w, dtype)
     torch.cuda.synchronize()
     assert torch.equal(comb.view(torch.int16), ref.view(torch.int16))
