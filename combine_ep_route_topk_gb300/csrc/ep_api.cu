@@ -274,6 +274,14 @@ ep_status_t ep_combine(const void* y, int32_t N, int32_t H, int32_t E, int32_t K
     return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
 }
 
+ep_status_t ep_selftest_wait_timeout(int32_t* status, void* workspace, size_t ws_bytes,
+                                     void* stream) {
+    if (!status || !workspace || ws_bytes < sizeof(unsigned)) return EP_ERR_INVALID_ARG;
+    if (!aligned4(status) || !aligned4(workspace)) return EP_ERR_INVALID_ARG;
+    return cuda_status(launch_barrier_selftest(static_cast<unsigned*>(workspace), status,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 const char* ep_status_string(ep_status_t status) {
     switch (status) {
         case EP_OK: return "EP_OK";

@@ -69,17 +69,19 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
     return v;
 }
 
-// Grid-wide barrier over a co-resident grid.  Returns false (after recording
-// the failure) if the wait ran out, which a cooperative launch rules out.
-__device__ bool grid_barrier(unsigned* ctr, int32_t* status) {
+// Grid-wide barrier over a co-resident grid: every block adds one to *ctr,
+// then waits until it reaches `target` (the grid size).  The wait is bounded
+// by `limit` polls; if it runs out the block records 1 in *status and the
+// barrier returns false, which a cooperative launch rules out.
+__device__ bool grid_barrier(unsigned* ctr, unsigned target, unsigned limit, int32_t* status) {
     __syncthreads();
     int ok = 1;
     if (threadIdx.x == 0) {
         __threadfence();
         atomicAdd(ctr, 1u);
         unsigned polls = 0;
-        while (ld_acquire_gpu(ctr) < gridDim.x) {
-            if (++polls > kSpinLimit) {
+        while (ld_acquire_gpu(ctr) < target) {
+            if (++polls > limit) {
                 ok = 0;
                 if (status) atomicExch(status, 1);
                 break;
@@ -89,6 +91,15 @@ __device__ bool grid_barrier(unsigned* ctr, int32_t* status) {
         __threadfence();
     }
     return __syncthreads_and(ok) != 0;
+}
+
+// Self-test of the bounded wait: a barrier that waits for one block more
+// than the grid has, so the wait runs out after `limit` polls, records 1 in
+// *status, and every block returns.
+__global__ void __launch_bounds__(32) barrier_timeout_kernel(unsigned* ctr, unsigned limit,
+                                                             int32_t* status) {
+    pdl_prologue();
+    grid_barrier(ctr, gridDim.x + 1, limit, status);
 }
 
 template <int VPL, bool VEC, int KT>
@@ -129,7 +140,7 @@ __global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
         for (int e = threadIdx.x; e < E; e += kNT) row[e] = s_w[e];
         __syncthreads();
     }
-    if (!grid_barrier(f.bar + 0, f.status)) return;
+    if (!grid_barrier(f.bar + 0, gridDim.x, kSpinLimit, f.status)) return;
 
     // ---- phase 2: tiles of 32 expert columns; warp w scans row group w, so
     // every row read is one coalesced 128-byte line per warp
@@ -175,7 +186,7 @@ __global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
         }
         __syncthreads();
     }
-    if (!grid_barrier(f.bar + 1, f.status)) return;
+    if (!grid_barrier(f.bar + 1, gridDim.x, kSpinLimit, f.status)) return;
 
     // ---- phase 3: offsets, side outputs, stable positions
     load_expert_offsets<kNT>(a.ws_totals, E, s_eoff, s_tmp);
@@ -206,6 +217,15 @@ cudaError_t launch_fused_t(FusedArgs& f, int C, int slots, size_t smem, cudaStre
 }
 
 }  // namespace
+
+cudaError_t launch_barrier_selftest(unsigned* ctr, int32_t* status, cudaStream_t s) {
+    cudaError_t err = cudaMemsetAsync(ctr, 0, sizeof(unsigned), s);
+    if (err == cudaSuccess) err = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
+    if (err == cudaSuccess)
+        err = launch(barrier_timeout_kernel, dim3(2), dim3(32), 0, s, ctr, 1u << 20, status);
+    note_launch();
+    return err;
+}
 
 cudaError_t launch_route_layout(const RouteLayoutArgs& r, cudaStream_t s, bool* launched) {
     *launched = false;

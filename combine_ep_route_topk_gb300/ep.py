@@ -53,6 +53,7 @@ def lib():
         L.ep_dispatch.argtypes = [P, i32, i32, i32, i32, P, P, P, ctypes.c_int, i32, ctypes.c_int,
                                   P, P, P]
         L.ep_combine.argtypes = [P, i32, i32, i32, i32, P, P, P, P, ctypes.c_int, i32, P, P]
+        L.ep_selftest_wait_timeout.argtypes = [P, P, sz, P]
         for f in ("ep_route_topk", "ep_expert_balance_map", "ep_dispatch_layout", "ep_dispatch",
                   "ep_combine"):
             getattr(L, f).restype = ctypes.c_int
@@ -256,3 +257,18 @@ def ep_combine(y, topk_idx, topk_w, pos, expert_offsets, E, layout=EP_LAYOUT_CON
         _opt(expert_offsets, torch.int32, "expert_offsets", (E + 1,)), layout, cap,
         _dev(out, torch.bfloat16, "out", (N, H)), _stream(stream)))
     return out
+
+
+def ep_selftest_wait_timeout(stream=None):
+    """Runs the bounded-wait self-test (a grid barrier that can never complete
+    gives up, sets the status word to 1 and returns).  Returns the device
+    status tensor (int32 [1]); read it after synchronising."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    _check("ep_selftest_wait_timeout", lib().ep_selftest_wait_timeout(
+        ctypes.c_void_p(status.data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+        _stream(stream)))
+    # keep the workspace alive until the kernel has run
+    ws.record_stream(torch.cuda.current_stream(dev) if stream is None else stream)
+    return status

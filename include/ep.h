@@ -257,6 +257,21 @@ ep_status_t ep_combine(const void* y, int32_t N, int32_t H, int32_t E, int32_t K
                        const int32_t* expert_offsets, ep_layout_t layout, int32_t cap,
                        void* out, void* stream);
 
+/*
+ * ep_selftest_wait_timeout -- no counterpart in the source pages: a check of
+ * the bounded wait that guards the grid barriers of ep_route_layout.  It
+ * launches a 2-block kernel whose barrier waits for a third block that never
+ * comes; the wait gives up after 2^20 polls (well under a second), the kernel
+ * sets *status to 1 and every block returns, leaving the context usable.
+ *   status     device int32, set to 0 before the kernel and 1 by it.
+ *   workspace  device memory of at least 4 bytes, 4-byte aligned (the
+ *              barrier counter; zeroed here).
+ * Returns EP_ERR_INVALID_ARG (nothing launched) for a NULL or misaligned
+ * pointer or ws_bytes < 4, EP_ERR_CUDA on a launch failure.
+ */
+ep_status_t ep_selftest_wait_timeout(int32_t* status, void* workspace, size_t ws_bytes,
+                                     void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* ep_status_string(ep_status_t status);
 

@@ -100,6 +100,15 @@ def test_dispatch_and_combine_argument_checks(L):
     assert L.ep_kernel_launch_count() == 0
 
 
+def test_selftest_argument_checks(L):
+    f = L.ep_selftest_wait_timeout
+    assert f(None, p(), 256, None) == INVALID
+    assert f(p(), None, 256, None) == INVALID
+    assert f(p(), p(), 3, None) == INVALID        # room for the counter
+    assert f(p(4098), p(), 256, None) == INVALID  # status not 4-byte aligned
+    assert L.ep_kernel_launch_count() == 0
+
+
 def test_binding_refuses_cpu_tensors(L):
     import torch
     with pytest.raises(ep.EPError):
