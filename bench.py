@@ -467,22 +467,31 @@ def run_ours(args, world, rank, local):
 
 
 def two_batch_overlap(args, ep, torch, dev, main_stream, inp, w, flush, dist):
-    """The same batch as two micro-batches (ranks 0..R/2-1 and R/2..R-1) on two
-    streams (pipeline.two_batch_overlap): one micro-batch's latency-bound
-    routing and layout overlap the other's HBM-bound dispatch and combine."""
+    """The same batch as micro-batches of contiguous rank groups, each on its
+    own stream (pipeline.two_batch_overlap): one micro-batch's latency-bound
+    routing and layout overlap another's HBM-bound dispatch and combine.
+    Even halves, and a one-rank first group (only its routing and layout are
+    exposed)."""
     from combine_ep_route_topk_gb300 import pipeline as pl
-    K, H = w.K, w.H
+    K, H, R = w.K, w.H, w.R
     comb = torch.empty(inp["N"], H, dtype=torch.bfloat16, device=dev)
-    mbs = pl.make_micro_batches(inp["logits"], inp["x"], inp["rank_offsets"], K,
-                                ep.EP_DTYPE_FP8_E4M3_B128, comb)
     y = inp["y"]
+    out = {}
+    for name, groups in (("even_halves", [(0, R // 2), (R // 2, R)]),
+                         ("first_rank_alone", [(0, 1), (1, R)])):
+        mbs = pl.make_micro_batches(inp["logits"], inp["x"], inp["rank_offsets"], K,
+                                    ep.EP_DTYPE_FP8_E4M3_B128, comb, rank_groups=groups)
 
-    def step():
-        pl.two_batch_overlap(mbs, K, ep.EP_DTYPE_FP8_E4M3_B128,
-                             lambda mb: y[mb.t0 * K:mb.t1 * K], main_stream)
+        def step():
+            pl.two_batch_overlap(mbs, K, ep.EP_DTYPE_FP8_E4M3_B128,
+                                 lambda mb: y[mb.t0 * K:mb.t1 * K], main_stream)
 
-    return _time_schedule(args, torch, main_stream, flush, dist, step, inp["N"],
-                          "ranks 0..3 and 4..7 as two micro-batches on two streams")
+        out[name] = _time_schedule(
+            args, torch, main_stream, flush, dist, step, inp["N"],
+            "micro-batches of ranks " + ", ".join(f"{a}..{b - 1}" for a, b in groups) +
+            " on their own streams")
+        del mbs
+    return out
 
 
 def chunked_prefill(args, ep, torch, dev, main_stream, inp, w, flush, dist, T=8192):

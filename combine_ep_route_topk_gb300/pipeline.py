@@ -64,14 +64,24 @@ def split_by_ranks(rank_offsets_host, parts=2):
     return [(bounds[i], bounds[i + 1]) for i in range(parts) if bounds[i] < bounds[i + 1]]
 
 
-def make_micro_batches(logits, x, rank_offsets, K, dtype, comb, parts=2):
-    """Buffers for `parts` micro-batches of contiguous rank groups."""
+def make_micro_batches(logits, x, rank_offsets, K, dtype, comb, parts=2, rank_groups=None):
+    """Buffers for `parts` micro-batches of contiguous rank groups (ranks split
+    evenly), or for the groups [(rank_lo, rank_hi)] given in `rank_groups`,
+    which must tile 0..R in order (an uneven split, e.g. a small first group
+    whose routing and layout are the only ones not hidden under another
+    micro-batch's dispatch and combine)."""
     dev = logits.device
     E = logits.shape[1]
     H = x.shape[1]
     offs = rank_offsets.cpu().tolist()
+    R = len(offs) - 1
+    groups = split_by_ranks(offs, parts) if rank_groups is None else list(rank_groups)
+    if (not groups or groups[0][0] != 0 or groups[-1][1] != R or
+            any(a[1] != b[0] for a, b in zip(groups, groups[1:])) or
+            any(lo >= hi for lo, hi in groups)):
+        raise ValueError(f"rank groups {groups} do not tile ranks 0..{R} in order")
     mbs = []
-    for lo, hi in split_by_ranks(offs, parts):
+    for lo, hi in groups:
         t0, t1 = offs[lo], offs[hi]
         n = t1 - t0
         ro = torch.tensor([o - t0 for o in offs[lo:hi + 1]], dtype=torch.int32, device=dev)

@@ -48,7 +48,8 @@ def _single_batch(inp, w, dtype):
 
 @pytest.mark.parametrize("name,dtype", [("lumpy", ep.EP_DTYPE_BF16),
                                         ("prefill", ep.EP_DTYPE_FP8_E4M3_B128)])
-def test_two_batch_overlap_matches_single_batch(name, dtype):
+@pytest.mark.parametrize("groups", [None, [(0, 1), (1, 8)], [(0, 1), (1, 3), (3, 8)]])
+def test_two_batch_overlap_matches_single_batch(name, dtype, groups):
     w = wl.WORKLOADS[name]
     if name == "prefill":
         w = w.scaled(batch=("uniform", 200, 300))
@@ -56,8 +57,10 @@ def test_two_batch_overlap_matches_single_batch(name, dtype):
     N, E, K, H = inp["N"], w.E, w.K, w.H
     logits, x, ro = inp["logits"].cuda(), inp["x"].cuda(), inp["rank_offsets"].cuda()
     comb = torch.empty(N, H, dtype=torch.bfloat16, device="cuda")
-    mbs = pl.make_micro_batches(logits, x, ro, K, dtype, comb)
-    assert len(mbs) == 2 and mbs[0].t1 == mbs[1].t0
+    mbs = pl.make_micro_batches(logits, x, ro, K, dtype, comb, rank_groups=groups)
+    assert len(mbs) == (2 if groups is None else len(groups))
+    assert mbs[0].t0 == 0 and mbs[-1].t1 == N
+    assert all(a.t1 == b.t0 for a, b in zip(mbs, mbs[1:]))
     pl.two_batch_overlap(mbs, K, dtype,
                          lambda mb: _scaled(mb.out, mb.scales, mb.lay, E, (mb.t1 - mb.t0) * K))
     torch.cuda.synchronize()
