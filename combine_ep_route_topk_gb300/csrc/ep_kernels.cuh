@@ -100,12 +100,11 @@ struct RouteLayoutArgs {
     int32_t* status;         // device int32 or nullptr
     int32_t* workspace;
 };
-// Self-test of the fused kernel's bounded grid-barrier wait (route_layout.cu).
-cudaError_t launch_barrier_selftest(unsigned* ctr, int32_t* status, cudaStream_t s);
-
 // *launched is false when the sizes have no fused instance or the device
 // cannot hold a block of it; the caller then runs route and layout kernels.
 cudaError_t launch_route_layout(const RouteLayoutArgs& r, cudaStream_t s, bool* launched);
+// Self-test of the fused kernel's bounded grid-barrier wait (route_layout.cu).
+cudaError_t launch_barrier_selftest(unsigned* ctr, int32_t* status, cudaStream_t s);
 
 // ---- dispatch / combine --------------------------------------------------
 struct MoveArgs {
