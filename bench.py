@@ -304,64 +304,81 @@ def run_ours(args, world, rank, local):
     dc_ms *= args.steps / n_bd
 
     # ---- end to end through the public API, host buffers --------------------
-    # Inputs start in pinned host memory and the result goes back to it; the
-    # copies are inside the timed region.  Headline: HostPipeline, whose
-    # copies in overlap the previous step's kernels and copy out.  Beside it,
-    # the latency of one step run alone (copies in, kernels, copy out).
-    # Host-link bandwidth is shared with the machine's other users and drifts,
-    # so the two schedules alternate in windows and each reports its median
-    # window.
-    n_win = 3
-    e2e_steps = max(2, min(args.steps, 24) // n_win)  # steps per window
-    def pinned_copy(t):
-        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        h.copy_(t)
-        return h
-    x_h, lg_h, ro_h, y_h = (pinned_copy(t) for t in (x, logits, ro, y))
-    outs_h = [torch.empty(N, H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    h2d = x_h.numel() * 2 + lg_h.numel() * 4 + ro_h.numel() * 4 + y_h.numel() * 2
-    d2h = outs_h[0].numel() * 2
-    hp = HostPipeline(N, E, K, H, R, dtype, dev, cap=cap, expert_map=emap)
-    torch.cuda.synchronize()
-
-    def pipelined_window(n):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(dist)
-        a.record(stream)
-        for i in range(n):
-            hp.step(x_h, lg_h, ro_h, y_h, outs_h[i % 2])
-        hp.join(stream)
-        b.record(stream)
+    e2e_line = None
+    if not args.no_e2e:
+        # Inputs start in pinned host memory and the result goes back to it; the
+        # copies are inside the timed region.  Headline: HostPipeline, whose
+        # copies in overlap the previous step's kernels and copy out.  Beside it,
+        # the latency of one step run alone (copies in, kernels, copy out).
+        # Host-link bandwidth is shared with the machine's other users and drifts,
+        # so the two schedules alternate in windows and each reports its median
+        # window.
+        n_win = 3
+        e2e_steps = max(2, min(args.steps, 24) // n_win)  # steps per window
+        def pinned_copy(t):
+            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            h.copy_(t)
+            return h
+        x_h, lg_h, ro_h, y_h = (pinned_copy(t) for t in (x, logits, ro, y))
+        outs_h = [torch.empty(N, H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        h2d = x_h.numel() * 2 + lg_h.numel() * 4 + ro_h.numel() * 4 + y_h.numel() * 2
+        d2h = outs_h[0].numel() * 2
+        hp = HostPipeline(N, E, K, H, R, dtype, dev, cap=cap, expert_map=emap)
         torch.cuda.synchronize()
-        barrier(dist)
-        return max_over_ranks(dist, a.elapsed_time(b))
 
-    def serial_window(n):
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(n)]
-        barrier(dist)
-        for a, b in ev:
+        def pipelined_window(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier(dist)
             a.record(stream)
-            x.copy_(x_h, non_blocking=True)
-            logits.copy_(lg_h, non_blocking=True)
-            ro.copy_(ro_h, non_blocking=True)
-            y.copy_(y_h, non_blocking=True)
-            step()
-            outs_h[0].copy_(comb, non_blocking=True)
+            for i in range(n):
+                hp.step(x_h, lg_h, ro_h, y_h, outs_h[i % 2])
+            hp.join(stream)
             b.record(stream)
-        torch.cuda.synchronize()
-        barrier(dist)
-        return max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in ev))
+            torch.cuda.synchronize()
+            barrier(dist)
+            return max_over_ranks(dist, a.elapsed_time(b))
 
-    pipelined_window(2)  # warm-up of both schedules
-    serial_window(1)
-    win_pipe, win_serial = [], []
-    for _ in range(n_win):
-        win_pipe.append(pipelined_window(e2e_steps))
-        win_serial.append(serial_window(e2e_steps))
-    e2e_ms = statistics.median(win_pipe)
-    serial_ms = statistics.median(win_serial)
-    del hp, x_h, lg_h, ro_h, y_h, outs_h
+        def serial_window(n):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(n)]
+            barrier(dist)
+            for a, b in ev:
+                a.record(stream)
+                x.copy_(x_h, non_blocking=True)
+                logits.copy_(lg_h, non_blocking=True)
+                ro.copy_(ro_h, non_blocking=True)
+                y.copy_(y_h, non_blocking=True)
+                step()
+                outs_h[0].copy_(comb, non_blocking=True)
+                b.record(stream)
+            torch.cuda.synchronize()
+            barrier(dist)
+            return max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in ev))
+
+        pipelined_window(2)  # warm-up of both schedules
+        serial_window(1)
+        win_pipe, win_serial = [], []
+        for _ in range(n_win):
+            win_pipe.append(pipelined_window(e2e_steps))
+            win_serial.append(serial_window(e2e_steps))
+        e2e_ms = statistics.median(win_pipe)
+        serial_ms = statistics.median(win_serial)
+        tok_step = N * world * e2e_steps
+        e2e_line = {
+            "value": round(tok_step / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_ms / e2e_steps, 3), "steps": e2e_steps * n_win,
+            "schedule": "pipeline.HostPipeline: step i+1's copies in overlap step i's "
+                        "kernels and copy out (double-buffered device inputs and result)",
+            "h2d_GB/s": round(h2d * e2e_steps / (e2e_ms / 1e3) / 1e9, 1),
+            "windows": f"{n_win} windows of {e2e_steps} steps, alternating with the "
+                       "serial schedule; median window",
+            "window_ms_per_step": [round(t / e2e_steps, 3) for t in win_pipe],
+            "serial": {"value": round(tok_step / (serial_ms / 1e3), 1),
+                       "ms_per_step": round(serial_ms / e2e_steps, 3),
+                       "window_ms_per_step": [round(t / e2e_steps, 3) for t in win_serial],
+                       "schedule": "one step alone: copies in, kernels, copy out"}}
+        del hp, x_h, lg_h, ro_h, y_h, outs_h
 
     # other schedules of the same batch, and the decode step (after the e2e
     # measurement, so their allocations and graphs cannot affect it)
@@ -442,19 +459,7 @@ def run_ours(args, world, rank, local):
         "two_batch_overlap": overlap,
         "chunked_rounds": chunk,
         "decode_step": decode,
-        "e2e": {"value": round(tok * e2e_steps / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms / e2e_steps, 3), "steps": e2e_steps * n_win,
-                "schedule": "pipeline.HostPipeline: step i+1's copies in overlap step i's "
-                            "kernels and copy out (double-buffered device inputs and result)",
-                "h2d_GB/s": round(h2d * e2e_steps / (e2e_ms / 1e3) / 1e9, 1),
-                "windows": f"{n_win} windows of {e2e_steps} steps, alternating with the "
-                           "serial schedule; median window",
-                "window_ms_per_step": [round(t / e2e_steps, 3) for t in win_pipe],
-                "serial": {"value": round(tok * e2e_steps / (serial_ms / 1e3), 1),
-                           "ms_per_step": round(serial_ms / e2e_steps, 3),
-                           "window_ms_per_step": [round(t / e2e_steps, 3) for t in win_serial],
-                           "schedule": "one step alone: copies in, kernels, copy out"}},
+        "e2e": e2e_line,
         "gpu_launches": int(launches),
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 3),
@@ -724,6 +729,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="prefill",
                     choices=["toy", "lumpy", "decode", "prefill", "skew"],
                     help="the workload a step runs (default: prefill, the headline)")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end host-buffer measurement (its pipeline holds "
+                         "about 11 GB more on the device); for profiling runs")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the overlap, chunked and decode measurements (profiling)")
     ap.add_argument("--decode-only", action="store_true",
