@@ -38,11 +38,11 @@ ep_status_t check_sizes(int32_t N, int32_t E, int32_t K) {
 
 int sm_count() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
     int n = g_sm_count[dev].load(std::memory_order_relaxed);
     if (n <= 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
+            n = 152;  // GB300
         g_sm_count[dev].store(n, std::memory_order_relaxed);
     }
     return n;
