@@ -492,3 +492,92 @@ def test_cuda_graph_capture_masked_decode():
         o = _oracle_chain(dict(inp, logits=new), w, EP_LAYOUT_MASKED, cap, EP_DTYPE_BF16)
         g = dict(idx=idx, w=wt, lay=lay, out=out, scales=None, comb=comb)
         _compare_chain(g, o, w, EP_LAYOUT_MASKED, cap, EP_DTYPE_BF16)
+
+
+@pytest.mark.parametrize("per_rank", [100, 600])  # one-cluster layout / three kernels
+def test_cuda_graph_capture_contiguous_fp8(per_rank):
+    """route -> layout -> FP8 contiguous dispatch -> combine captured once in
+    a CUDA graph and replayed on new logits, tokens and expert outputs copied
+    into the captured buffers; every replay matches the oracle."""
+    w = wl.WORKLOADS["prefill"].scaled(batch=("fixed", per_rank), H=1024)
+    inp = wl.make_inputs(w, seed=0)
+    N, E, K, R = inp["N"], w.E, w.K, w.R
+    logits, ro = inp["logits"].cuda(), inp["rank_offsets"].cuda()
+    x, y = inp["x"].cuda(), inp["y"].cuda()
+    idx = torch.empty(N, K, dtype=torch.int32, device="cuda")
+    wt = torch.empty(N, K, device="cuda")
+    from combine_ep_route_topk_gb300 import alloc_layout, ep_dispatch_layout_workspace_size
+    lay = alloc_layout(N, E, K, R, 0, "cuda")
+    ws = torch.empty(ep_dispatch_layout_workspace_size(N, E, K, R), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(N * K, w.H, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(N * K, w.H // 128, device="cuda")
+    comb = torch.empty(N, w.H, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def step():
+        ep_route_topk(logits, K, topk_idx=idx, topk_w=wt)
+        ep_dispatch_layout(idx, ro, E, 0, out=lay, workspace=ws)
+        ep_dispatch(x, idx, lay.pos, lay.expert_offsets, E, EP_LAYOUT_CONTIG, 0,
+                    EP_DTYPE_FP8_E4M3_B128, out=out, out_scales=sc)
+        ep_combine(y, idx, wt, lay.pos, lay.expert_offsets, E, EP_LAYOUT_CONTIG, 0, out=comb)
+
+    with torch.cuda.stream(s):
+        step()  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for seed in (21, 22):
+        new = wl.make_inputs(w, seed=seed)
+        # same rank sizes: the captured rank offsets stay valid
+        assert torch.equal(new["rank_offsets"], inp["rank_offsets"])
+        logits.copy_(new["logits"].cuda())
+        x.copy_(new["x"].cuda())
+        y.copy_(new["y"].cuda())
+        graph.replay()
+        torch.cuda.synchronize()
+        o = _oracle_chain(new, w, EP_LAYOUT_CONTIG, 0, EP_DTYPE_FP8_E4M3_B128)
+        g = dict(idx=idx, w=wt, lay=lay, out=out, scales=sc, comb=comb)
+        _compare_chain(g, o, w, EP_LAYOUT_CONTIG, 0, EP_DTYPE_FP8_E4M3_B128)
+
+
+def test_concurrent_host_threads_on_their_own_streams():
+    """Two host threads run the whole path on their own streams and inputs at
+    the same time, several times over: every result equals the one the same
+    inputs give alone (the library keeps no shared state on this path)."""
+    import threading
+    cases = []
+    for name, seed in (("lumpy", 1), ("skew", 2)):
+        w = wl.WORKLOADS[name]
+        inp = wl.make_inputs(w, seed=seed)
+        g = _gpu_chain(inp, w, EP_LAYOUT_CONTIG, 0, EP_DTYPE_BF16)
+        cases.append((w, {k: v.cuda() for k, v in inp.items() if torch.is_tensor(v)},
+                      {k: (v.clone() if torch.is_tensor(v) else v) for k, v in g.items()}))
+    errors = []
+
+    def worker(w, dev_inp, ref):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    idx, wt = ep_route_topk(dev_inp["logits"], w.K)
+                    lay = ep_dispatch_layout(idx, dev_inp["rank_offsets"], w.E)
+                    out, _ = ep_dispatch(dev_inp["x"], idx, lay.pos, lay.expert_offsets, w.E)
+                    comb = ep_combine(dev_inp["y"], idx, wt, lay.pos, lay.expert_offsets, w.E)
+                    s.synchronize()
+                    assert torch.equal(idx, ref["idx"]) and torch.equal(wt, ref["w"])
+                    assert torch.equal(lay.pos, ref["lay"].pos)
+                    assert torch.equal(out.view(torch.int16), ref["out"].view(torch.int16))
+                    assert torch.equal(comb.view(torch.int16), ref["comb"].view(torch.int16))
+        except Exception as exc:  # reported on the main thread
+            errors.append(repr(exc))
+
+    threads = [threading.Thread(target=worker, args=c) for c in cases]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    assert not any(t.is_alive() for t in threads)
+    assert not errors, errors
