@@ -150,7 +150,11 @@ size_t ep_dispatch_layout_workspace_size(int32_t N, int32_t E, int32_t K, int32_
  *                       cap, which the masked layout drops.
  *   workspace           device scratch of ws_bytes >= the size above; its
  *                       contents need no initialisation and are clobbered.
- * Three kernels; results are deterministic (no order depends on atomics).
+ * Problems of at most 16384 picks (N*K) and 64 ranks whose chunk rows fit in
+ * shared memory run as one launch of one thread-block cluster; larger ones as
+ * three kernels.  EP_LAYOUT_CLUSTER=0 in the environment (read at every call)
+ * selects the three kernels for every size.  Both give the same results, which
+ * are deterministic (no order depends on atomics).
  */
 ep_status_t ep_dispatch_layout(const int32_t* topk_idx, const int32_t* rank_offsets,
                                int32_t R, int32_t N, int32_t E, int32_t K, int32_t cap,
