@@ -651,6 +651,27 @@ def oracle_step(w, s):
                    cap=cap)
 
 
+def host_cpu():
+    """The host CPU as /proc/cpuinfo names it (the model name on x86; the
+    implementer and part numbers on Arm), the machine type and the core count."""
+    import platform
+    model = ""
+    try:
+        info = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = (t.strip() for t in line.split(":", 1))
+                    info.setdefault(k, v)
+        model = info.get("model name") or (
+            f"implementer {info['CPU implementer']} part {info['CPU part']}"
+            if "CPU implementer" in info and "CPU part" in info else "")
+    except OSError:
+        pass
+    return {"cpu": model or platform.processor() or "unknown", "machine": platform.machine(),
+            "host_cores": os.cpu_count()}
+
+
 def cpu_baseline(budget_s: float = 12.0):
     """The oracle as it stands, one thread, on sub-batches of the prefill
     workload (8 ranks x 256 tokens each) until about budget_s of CPU work."""
@@ -664,7 +685,7 @@ def cpu_baseline(budget_s: float = 12.0):
         total_tok += s["N"]
         reps += 1
     return {"value": round(total_tok / total_s, 1), "unit": "tokens/s", "cores": 1,
-            "kind": "oracle",
+            "kind": "oracle", **host_cpu(),
             "sample": f"one sub-batch of the prefill workload (8 ranks x {per_rank} tokens, "
                       f"E=256, K=8, H=7168; route, layout, FP8 dispatch, combine) run {reps} "
                       f"times: {total_tok} tokens in {total_s:.1f} s, single-threaded"}
@@ -709,7 +730,7 @@ def run_reference(args, world, rank):
         "config": {"workload": desc, "step": "route+layout+dispatch+combine",
                    "sample_per_step": sample},
         "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, **host_cpu()},
         "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
