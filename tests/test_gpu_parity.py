@@ -157,6 +157,23 @@ def test_layout_edge_cases(B, E, K, cap, layout_path):
     _check_layout(gpu, ref, cap)
 
 
+def test_worked_example_layout_on_gpu(layout_path):
+    """The CUDA layout of the worked table's routes equals the values derived
+    by hand from the pages (no oracle in between)."""
+    import test_oracle
+    g = test_oracle.read_worked_layout()
+    ro = torch.arange(5, dtype=torch.int32, device="cuda")
+    lay = ep_dispatch_layout(torch.from_numpy(g["picks"]).cuda(), ro, 16)
+    np.testing.assert_array_equal(np_(lay.expert_offsets), g["expert_offsets"])
+    np.testing.assert_array_equal(np_(lay.pos), g["pos"])
+    np.testing.assert_array_equal(np_(lay.row_src), g["row_src"])
+    np.testing.assert_array_equal(np_(lay.counts), g["counts"])
+    np.testing.assert_array_equal(np_(lay.rank_expert_offsets), g["rank_expert_offsets"])
+    masked = ep_dispatch_layout(torch.from_numpy(g["picks"]).cuda(), ro, 16, 1)
+    np.testing.assert_array_equal(np_(masked.masked_m), g["cap1_masked_m"])
+    assert int(np_(masked.overflow_count)[0]) == g["cap1_overflow"][0]
+
+
 def test_layout_all_tokens_one_expert_and_invalid_ids(layout_path):
     N, E, K = 300, 16, 2
     idx = np.zeros((N, K), np.int32)

@@ -28,6 +28,23 @@ def _read_worked_example():
     return np.array(rows, np.float32), np.array(picks, np.int32)
 
 
+def read_worked_layout():
+    """The hand-derived layout of the worked example's routes (golden)."""
+    d = {}
+    with open(os.path.join(GOLDEN, "worked_example_layout.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            key, *vals = line.split()
+            if key in ("picks", "pos"):
+                d.setdefault(key, []).append([int(v) for v in vals[1:]])
+            elif "[" in key:
+                d.setdefault(key.split("[")[0], []).append([int(v) for v in vals])
+            else:
+                d[key] = [int(v) for v in vals]
+    return {k: np.array(v, np.int32) for k, v in d.items()}
+
+
 def _bf16_bits(t):
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
@@ -463,3 +480,24 @@ def test_combine_float_chain_rounding_fixtures():
     lay2 = oracle.layout(idx2, np.array([0, 1], np.int32), 2)
     out2 = oracle.combine(y[:2], idx2, w2, lay2["pos"], lay2["expert_offsets"], 2)
     assert np.all(out2 == 0x3F80)
+
+
+# ------------------------------------------------------------ worked layout ---
+
+def test_worked_example_layout_by_hand():
+    """The layout of the worked table's routes (one token per rank), against
+    values derived by hand from the pages: counts, offsets, positions, row
+    sources, and the masked capacity-1 drop of expert 13's second row."""
+    g = read_worked_layout()
+    logits, picks = _read_worked_example()
+    np.testing.assert_array_equal(g["picks"], picks)  # the same routes as the table
+    ro = np.arange(5, dtype=np.int32)                  # ranks 0..3, one token each
+    lay = oracle.layout(g["picks"], ro, 16, 0)
+    np.testing.assert_array_equal(lay["expert_offsets"], g["expert_offsets"])
+    np.testing.assert_array_equal(lay["pos"], g["pos"])
+    np.testing.assert_array_equal(lay["row_src"], g["row_src"])
+    np.testing.assert_array_equal(lay["counts"], g["counts"])
+    np.testing.assert_array_equal(lay["rank_expert_offsets"], g["rank_expert_offsets"])
+    masked = oracle.layout(g["picks"], ro, 16, 1)
+    np.testing.assert_array_equal(masked["masked_m"], g["cap1_masked_m"])
+    assert masked["overflow"] == g["cap1_overflow"][0]
