@@ -114,3 +114,39 @@ def test_binding_refuses_cpu_tensors(L):
     with pytest.raises(ep.EPError):
         ep.ep_route_topk(torch.zeros(4, 16), 2, topk_idx=torch.zeros(4, 2, dtype=torch.int32),
                          topk_w=torch.zeros(4, 2))
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "ep.h"
+
+int main(void) {
+    /* argument checks only: nothing here reaches a GPU */
+    ep_status_t st = ep_route_topk((const float*)0, 10, 16, 17, 0, 0, 0, 0);  /* K > E */
+    if (st != EP_ERR_INVALID_ARG) return 1;
+    st = ep_dispatch((const void*)0, 4, 100, 16, 2, 0, 0, 0, EP_LAYOUT_CONTIG, 0,
+                     EP_DTYPE_BF16, 0, 0, 0);  /* H % 8 != 0 */
+    if (st != EP_ERR_INVALID_ARG) return 2;
+    if (ep_abi_version() != 1) return 3;
+    if (ep_dispatch_layout_workspace_size(32768, 256, 8, 8) == 0) return 4;
+    if (ep_kernel_launch_count() != 0) return 5;
+    printf("%s\n", ep_status_string(EP_ERR_UNSUPPORTED));
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(L, tmp_path):
+    """include/ep.h compiles as C11 with warnings as errors, and a C program
+    links against libep_gb300.so and gets the documented status codes."""
+    import subprocess
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(ep.LIB_PATH)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                    "-L", libdir, "-lep_gb300", f"-Wl,-rpath,{libdir}"], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    assert r.stdout.strip() == "EP_ERR_UNSUPPORTED"
