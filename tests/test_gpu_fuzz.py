@@ -1,0 +1,102 @@
+"""Seeded random configurations of the whole path against the CPU oracle,
+stage by stage, so that no stage's inputs come from the CUDA path:
+  - route: random E, K (E not a multiple of 32, odd K, K = E), ties;
+  - layout: random ranks (empty ones, up to 70), capacities, on both layout
+    implementations (one cluster, three kernels);
+  - dispatch: bf16 or FP8 rows, contiguous or masked, from the oracle's layout;
+  - combine: from the oracle's weights and layout, bit-exact.
+Sizes are small so that the oracle finishes in seconds."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_ep_route_topk_gb300 import (EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3_B128, EP_LAYOUT_CONTIG,
+                                         EP_LAYOUT_MASKED, ep_combine, ep_dispatch,
+                                         ep_dispatch_layout, ep_route_topk)
+
+from _util import bits, np_, weight_rtol
+
+pytestmark = pytest.mark.gpu
+
+
+def _config(rng):
+    K = int(rng.integers(1, 33))
+    E = int(rng.integers(K, 300)) if rng.random() < 0.8 else K
+    R = int(rng.integers(1, 71))
+    B = rng.integers(0, 41, size=R)
+    B[rng.random(R) < 0.2] = 0  # some empty ranks
+    fp8 = rng.random() < 0.4
+    H = int(rng.choice([128, 256, 384])) if fp8 else 8 * int(rng.integers(1, 66))
+    masked = rng.random() < 0.4
+    cap = int(rng.integers(1, 12)) if masked else 0
+    return E, K, R, B, H, fp8, masked, cap
+
+
+@pytest.mark.parametrize("seed", range(200))
+def test_random_configuration(seed, monkeypatch):
+    rng = np.random.default_rng(1000 + seed)
+    E, K, R, B, H, fp8, masked, cap = _config(rng)
+    N = int(B.sum())
+    offs = np.concatenate([[0], np.cumsum(B)]).astype(np.int32)
+    g = torch.Generator().manual_seed(seed)
+    logits = torch.randn(N, E, generator=g)
+    if rng.random() < 0.3:  # coarse values: many exact ties
+        logits = torch.round(logits * 2) / 2
+    x = (torch.randn(N, H, generator=g) * 4).to(torch.bfloat16)
+    layout = EP_LAYOUT_MASKED if masked else EP_LAYOUT_CONTIG
+    dtype = EP_DTYPE_FP8_E4M3_B128 if fp8 else EP_DTYPE_BF16
+
+    # route
+    oidx, ow = oracle.route_topk(logits.numpy(), K)
+    idx, w = ep_route_topk(logits.cuda(), K)
+    np.testing.assert_array_equal(np_(idx), oidx)
+    np.testing.assert_allclose(np_(w), ow, rtol=weight_rtol())
+
+    # layout of the oracle's picks, both implementations
+    olay = oracle.layout(oidx, offs, E, cap)
+    for path in ("cluster", "kernels"):
+        if path == "kernels":
+            monkeypatch.setenv("EP_LAYOUT_CLUSTER", "0")
+        else:
+            monkeypatch.delenv("EP_LAYOUT_CLUSTER", raising=False)
+        lay = ep_dispatch_layout(torch.from_numpy(oidx).cuda(), torch.from_numpy(offs).cuda(),
+                                 E, cap)
+        for name in ("counts", "expert_offsets", "rank_expert_offsets", "pos", "row_src"):
+            np.testing.assert_array_equal(np_(getattr(lay, name)), olay[name],
+                                          err_msg=f"{name} ({path})")
+        if cap:
+            np.testing.assert_array_equal(np_(lay.masked_m), olay["masked_m"])
+            assert int(np_(lay.overflow_count)[0]) == olay["overflow"]
+    monkeypatch.delenv("EP_LAYOUT_CLUSTER", raising=False)
+
+    # dispatch from the oracle's layout
+    pos_d = torch.from_numpy(olay["pos"]).cuda()
+    eoff_d = torch.from_numpy(olay["expert_offsets"]).cuda()
+    idx_d = torch.from_numpy(oidx).cuda()
+    oout, osc = oracle.dispatch(bits(x), oidx, olay["pos"], olay["expert_offsets"], E,
+                                layout=layout, cap=cap, dtype=dtype)
+    out, sc = ep_dispatch(x.cuda(), idx_d, pos_d, eoff_d, E, layout, cap, dtype)
+    got = bits(out) if dtype == EP_DTYPE_BF16 else np_(out)
+    if masked:  # rows past masked_m are unspecified
+        gm, om = got.reshape(E, cap, H), oout.reshape(E, cap, H)
+        for e in range(E):
+            m = olay["masked_m"][e]
+            np.testing.assert_array_equal(gm[e, :m], om[e, :m])
+            if fp8:
+                np.testing.assert_array_equal(
+                    np_(sc).reshape(E, cap, -1)[e, :m].view(np.uint32),
+                    osc.reshape(E, cap, -1)[e, :m].view(np.uint32))
+    else:
+        np.testing.assert_array_equal(got, oout)
+        if fp8:
+            np.testing.assert_array_equal(np_(sc).view(np.uint32), osc.view(np.uint32))
+
+    # combine of random expert outputs with the oracle's weights and layout
+    rows = N * K if not masked else E * cap
+    y = torch.randn(rows, H, generator=g).to(torch.bfloat16)
+    ocomb = oracle.combine(bits(y), oidx, ow, olay["pos"], olay["expert_offsets"], E,
+                           layout=layout, cap=cap)
+    comb = ep_combine(y.cuda(), idx_d, torch.from_numpy(ow).cuda(), pos_d, eoff_d, E, layout,
+                      cap)
+    np.testing.assert_array_equal(bits(comb), ocomb)
