@@ -100,3 +100,41 @@ def test_random_configuration(seed, monkeypatch):
     comb = ep_combine(y.cuda(), idx_d, torch.from_numpy(ow).cuda(), pos_d, eoff_d, E, layout,
                       cap)
     np.testing.assert_array_equal(bits(comb), ocomb)
+
+
+@pytest.mark.parametrize("seed", range(80))
+def test_random_fused_route_layout(seed):
+    """ep_route_layout (one cooperative kernel where an instance exists, else
+    route + layout) on random sizes, including E of 128 / 256 / 512 / 1024
+    (16-byte loads) and the scalar instances, against the oracle's route
+    then layout; the status word stays 0."""
+    from combine_ep_route_topk_gb300 import ep_route_layout
+    rng = np.random.default_rng(5000 + seed)
+    K = int(rng.integers(1, 33))
+    E = int(rng.choice([128, 256, 512, 1024])) if rng.random() < 0.5 else \
+        int(rng.integers(K, 300))
+    E = max(E, K)
+    R = int(rng.integers(1, 71))
+    B = rng.integers(0, 60, size=R)
+    B[rng.random(R) < 0.2] = 0
+    cap = int(rng.integers(1, 12)) if rng.random() < 0.4 else 0
+    N = int(B.sum())
+    offs = np.concatenate([[0], np.cumsum(B)]).astype(np.int32)
+    g = torch.Generator().manual_seed(7000 + seed)
+    logits = torch.randn(N, E, generator=g)
+    if rng.random() < 0.3:
+        logits = torch.round(logits * 2) / 2
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    idx, w, lay = ep_route_layout(logits.cuda(), torch.from_numpy(offs).cuda(), K, cap,
+                                  status=status)
+    torch.cuda.synchronize()
+    oidx, ow = oracle.route_topk(logits.numpy(), K)
+    olay = oracle.layout(oidx, offs, E, cap)
+    np.testing.assert_array_equal(np_(idx), oidx)
+    np.testing.assert_allclose(np_(w), ow, rtol=weight_rtol())
+    for name in ("counts", "expert_offsets", "rank_expert_offsets", "pos", "row_src"):
+        np.testing.assert_array_equal(np_(getattr(lay, name)), olay[name], err_msg=name)
+    if cap:
+        np.testing.assert_array_equal(np_(lay.masked_m), olay["masked_m"])
+        assert int(np_(lay.overflow_count)[0]) == olay["overflow"]
+    assert int(status.item()) == 0  # the call completed (fused or two kernels)
