@@ -89,7 +89,9 @@ static int logit_order(const void* pa, const void* pb) {
  * selected logits, w_k = exp(l_k - l_0) / sum_j exp(l_j - l_0), in double.
  * [P2] "Load balancing across GPUs": after experts are renumbered, the gate
  * must emit the new ids, so an optional expert_map[old] = new is applied to
- * the chosen ids without changing their order.
+ * the chosen ids without changing their order.  A map entry outside [0,E)
+ * gives "no pick" (-1), as an invalid id does everywhere on this path (the
+ * pages give no map format; the weights are those of the chosen logits).
  */
 void oracle_route_topk(const float* logits, int64_t N, int32_t E, int32_t K,
                        const int32_t* expert_map, int32_t* topk_idx, float* topk_w) {
@@ -109,7 +111,8 @@ void oracle_route_topk(const float* logits, int64_t N, int32_t E, int32_t K,
         }
         for (int32_t k = 0; k < K; ++k) {
             int32_t e = row[k].e;
-            topk_idx[t * K + k] = expert_map ? expert_map[e] : e;
+            int32_t id = expert_map ? expert_map[e] : e;
+            topk_idx[t * K + k] = (id >= 0 && id < E) ? id : -1;
             topk_w[t * K + k] = (float)(ex[k] / sum);
         }
     }

@@ -138,3 +138,36 @@ def test_random_fused_route_layout(seed):
         np.testing.assert_array_equal(np_(lay.masked_m), olay["masked_m"])
         assert int(np_(lay.overflow_count)[0]) == olay["overflow"]
     assert int(status.item()) == 0  # the call completed (fused or two kernels)
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_balance_map_and_expert_map(seed):
+    """Balanced renumbering on random count matrices (ties, idle experts,
+    counts near the int32 limit) equals the oracle's greedy; routing through
+    a random map with some out-of-range entries gives the oracle's picks."""
+    from combine_ep_route_topk_gb300 import ep_expert_balance_map
+    rng = np.random.default_rng(9000 + seed)
+    R = int(rng.choice([1, 2, 3, 4, 8, 16, 32, 64]))
+    E = R * int(rng.integers(1, max(2, 1024 // R) + 1))
+    E = min(E, 1024 - (1024 % R))
+    kind = seed % 3
+    if kind == 0:
+        counts = rng.integers(0, 1000, size=(R, E))
+    elif kind == 1:  # few distinct values: many frequency ties
+        counts = rng.integers(0, 3, size=(R, E)) * 5
+    else:  # large counts: totals near the int32 limit
+        counts = rng.integers(0, (2 ** 31 - 1) // max(1, R), size=(R, E))
+    counts = counts.astype(np.int32)
+    counts[:, rng.random(E) < 0.2] = 0
+    got = ep_expert_balance_map(torch.from_numpy(counts).cuda())
+    np.testing.assert_array_equal(np_(got), oracle.balance_map(counts))
+
+    K = int(rng.integers(1, min(E, 32) + 1))
+    emap = rng.permutation(E).astype(np.int32)
+    emap[rng.random(E) < 0.05] = E + 3  # out of range: those picks become "no pick"
+    g = torch.Generator().manual_seed(9000 + seed)
+    logits = torch.randn(97, E, generator=g)
+    idx, w = ep_route_topk(logits.cuda(), K, expert_map=torch.from_numpy(emap).cuda())
+    oidx, ow = oracle.route_topk(logits.numpy(), K, expert_map=emap)
+    np.testing.assert_array_equal(np_(idx), oidx)
+    np.testing.assert_allclose(np_(w), ow, rtol=weight_rtol())

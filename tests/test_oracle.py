@@ -112,6 +112,22 @@ def test_topk_bruteforce_with_ties():
                     np.testing.assert_allclose(w[t], ref, rtol=2 ** -23)
 
 
+def test_topk_expert_map_entry_out_of_range_is_no_pick():
+    """A renumbering map entry outside [0,E) gives "no pick" (-1) for that
+    pick; the selection and the weights are those of the logits.  By hand:
+    row [0, 3, 1, 2] picks experts 1 then 3 (logit gap 1), so the weights are
+    sigma(1) and 1 - sigma(1); map 1 -> 7 (out of range), 3 -> 1."""
+    logits = np.array([[0.0, 3.0, 1.0, 2.0]], np.float32)
+    emap = np.array([0, 7, 2, 1], np.int32)
+    idx, w = oracle.route_topk(logits, 2, expert_map=emap)
+    np.testing.assert_array_equal(idx, [[-1, 1]])
+    s1 = 1.0 / (1.0 + np.exp(-1.0))
+    np.testing.assert_allclose(w, [[s1, 1.0 - s1]], rtol=1e-6)
+    emap[1] = -5
+    idx, _ = oracle.route_topk(logits, 2, expert_map=emap)
+    np.testing.assert_array_equal(idx, [[-1, 1]])
+
+
 def test_topk_expert_map_applied_after_selection():
     g = torch.Generator().manual_seed(3)
     logits = torch.randn(50, 32, generator=g).numpy()

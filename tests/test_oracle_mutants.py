@@ -19,8 +19,10 @@ MUTANTS = [
     ("weight sum drops the first pick", "sum += ex[k];", "sum += k ? ex[k] : 0.0;"),
     ("weight exponent sign", "ex[k] = exp((double)row[k].v - top);",
      "ex[k] = exp(top - (double)row[k].v);"),
-    ("expert map ignored", "topk_idx[t * K + k] = expert_map ? expert_map[e] : e;",
-     "topk_idx[t * K + k] = e;"),
+    ("expert map ignored", "int32_t id = expert_map ? expert_map[e] : e;",
+     "int32_t id = e;"),
+    ("out-of-range map entries kept", "topk_idx[t * K + k] = (id >= 0 && id < E) ? id : -1;",
+     "topk_idx[t * K + k] = id;"),
     ("greedy ties to the higher set", "if (best < 0 || load[s] < load[best]) best = s;",
      "if (best < 0 || load[s] <= load[best]) best = s;"),
     ("layout: tokens in reverse within an expert",
