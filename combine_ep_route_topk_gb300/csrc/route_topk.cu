@@ -61,7 +61,10 @@ balance_map_kernel(const int32_t* __restrict__ counts, int R, int E, int32_t* __
     const int tid = threadIdx.x;
     int P = 1;
     while (P < E) P <<= 1;
-    // key ascending = (frequency descending, id ascending); 10 id bits
+    // key ascending = (frequency descending, id ascending): 10 id bits under
+    // 41 frequency bits (R <= 1024 counts below 2^31 sum to less than 2^41,
+    // so every frequency is exact)
+    constexpr long long kFreqTop = (1ll << 41) - 1;
     for (int e = tid; e < P; e += blockDim.x) {
         unsigned long long key = ~0ull;
         if (e < E) {
@@ -70,8 +73,7 @@ balance_map_kernel(const int32_t* __restrict__ counts, int R, int E, int32_t* __
                 const int c = counts[(size_t)r * E + e];
                 f += c > 0 ? c : 0;
             }
-            if (f > 0xffffffffll) f = 0xffffffffll;
-            key = ((unsigned long long)(0xffffffffll - f) << 10) | (unsigned long long)e;
+            key = ((unsigned long long)(kFreqTop - f) << 10) | (unsigned long long)e;
         }
         s_key[e] = key;
     }
@@ -101,7 +103,7 @@ balance_map_kernel(const int32_t* __restrict__ counts, int R, int E, int32_t* __
     for (int i = 0; i < E; ++i) {
         const unsigned long long key = s_key[i];
         const int e = (int)(key & 1023ull);
-        const long long f = 0xffffffffll - (long long)(key >> 10);
+        const long long f = kFreqTop - (long long)(key >> 10);
         long long bl = LLONG_MAX;
         int bs = INT_MAX;
         for (int s = tid; s < R; s += 32) {

@@ -143,20 +143,23 @@ def test_random_fused_route_layout(seed):
 @pytest.mark.parametrize("seed", range(60))
 def test_random_balance_map_and_expert_map(seed):
     """Balanced renumbering on random count matrices (ties, idle experts,
-    counts near the int32 limit) equals the oracle's greedy; routing through
+    counts near the int32 limit, frequencies past 2^32) equals the oracle's
+    greedy; routing through
     a random map with some out-of-range entries gives the oracle's picks."""
     from combine_ep_route_topk_gb300 import ep_expert_balance_map
     rng = np.random.default_rng(9000 + seed)
-    R = int(rng.choice([1, 2, 3, 4, 8, 16, 32, 64]))
+    R = int(rng.choice([1, 2, 3, 4, 8, 16, 32, 64, 1024]))
     E = R * int(rng.integers(1, max(2, 1024 // R) + 1))
     E = min(E, 1024 - (1024 % R))
-    kind = seed % 3
+    kind = seed % 4
     if kind == 0:
         counts = rng.integers(0, 1000, size=(R, E))
     elif kind == 1:  # few distinct values: many frequency ties
         counts = rng.integers(0, 3, size=(R, E)) * 5
-    else:  # large counts: totals near the int32 limit
+    elif kind == 2:  # large counts: totals near the int32 limit
         counts = rng.integers(0, (2 ** 31 - 1) // max(1, R), size=(R, E))
+    else:  # every count near the int32 limit: frequencies up to R * 2^31
+        counts = rng.integers(2 ** 31 - 64, 2 ** 31, size=(R, E))
     counts = counts.astype(np.int32)
     counts[:, rng.random(E) < 0.2] = 0
     got = ep_expert_balance_map(torch.from_numpy(counts).cuda())
