@@ -225,7 +225,9 @@ ep_status_t ep_dispatch_layout_static(const int32_t* topk_idx, const int32_t* ra
  * once and written K times.
  *   x              bf16 [N, H], 16-byte aligned; H % 8 == 0.
  *   topk_idx, pos, expert_offsets: as produced by ep_dispatch_layout.
- *   layout CONTIG: out rows = N*K, row of pick (t,k) = pos[t,k].
+ *   layout CONTIG: out rows = N*K, row of pick (t,k) = pos[t,k].  When
+ *                  some picks are "no pick", the rows from expert_offsets[E]
+ *                  on receive nothing and are not written.
  *   layout MASKED: out is [E, cap, H]; slot = pos[t,k] - expert_offsets[e];
  *                  delivered to (e, slot) when slot < cap, else dropped.
  *                  Rows at or past masked_m[e] are not written.
