@@ -87,6 +87,22 @@ def test_route_topk_expert_map():
     np.testing.assert_allclose(np_(w), ref_w, rtol=weight_rtol())
 
 
+@pytest.mark.parametrize("E,K", [(128, 4), (256, 8), (1024, 8)])
+def test_route_topk_logits_not_16_byte_aligned(E, K):
+    """Logits that start 4 bytes past a 16-byte boundary (legal: 4-byte
+    aligned) take the scalar-load kernels; same picks and weights."""
+    g = torch.Generator().manual_seed(E + K)
+    N = 203
+    flat = torch.randn(N * E + 1, generator=g)
+    dev = flat.cuda()
+    logits = dev[1:].view(N, E)
+    assert logits.data_ptr() % 16 == 4
+    idx, w = ep_route_topk(logits, K)
+    ref_idx, ref_w = oracle.route_topk(flat[1:].view(N, E).numpy(), K)
+    np.testing.assert_array_equal(np_(idx), ref_idx)
+    np.testing.assert_allclose(np_(w), ref_w, rtol=weight_rtol())
+
+
 @pytest.mark.parametrize("N", [1, 2, 15, 17])
 def test_route_topk_few_tokens(N):
     """Fewer tokens than one block serves (one or two tokens per warp)."""
