@@ -294,6 +294,23 @@ def test_layout_invalid_ids_are_not_picks():
     assert got["expert_offsets"][-1] == 5
 
 
+@pytest.mark.parametrize("seed", range(100))
+def test_layout_random_picks_match_stable_argsort(seed):
+    """Random picks (any ids, including -1, E and beyond, and the same expert
+    twice in a token), random ranks with empty ones, random capacities."""
+    rng = np.random.default_rng(300 + seed)
+    E = int(rng.integers(1, 70))
+    K = int(rng.integers(1, 9))
+    R = int(rng.integers(1, 12))
+    B = rng.integers(0, 30, size=R)
+    B[rng.random(R) < 0.25] = 0
+    N = int(B.sum())
+    offs = np.concatenate([[0], np.cumsum(B)]).astype(np.int32)
+    idx = rng.integers(-2, E + 3, size=(N, K)).astype(np.int32)
+    cap = int(rng.integers(1, 6)) if rng.random() < 0.5 else 0
+    _check_layout(oracle.layout(idx, offs, E, cap), _ref_layout(idx, offs, E, cap))
+
+
 # --------------------------------------------------------------- dispatch ---
 
 def test_dispatch_bf16_contig_and_masked():
