@@ -368,8 +368,9 @@ def run_ours(args, world, rank, local):
             "value": round(tok_step / (e2e_ms / 1e3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms / e2e_steps, 3), "steps": e2e_steps * n_win,
-            "schedule": "pipeline.HostPipeline: step i+1's copies in overlap step i's "
-                        "kernels and copy out (double-buffered device inputs and result)",
+            "schedule": "ep_host_pipeline_* (C ABI, via pipeline.HostPipeline): step i+1's "
+                        "copies in overlap step i's kernels and copy out (double-buffered "
+                        "device inputs and result)",
             "h2d_GB/s": round(h2d * e2e_steps / (e2e_ms / 1e3) / 1e9, 1),
             "windows": f"{n_win} windows of {e2e_steps} steps, alternating with the "
                        "serial schedule; median window",

@@ -16,6 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libep_gb300.so")
 SOURCES = ["ep_api.cu", "route_topk.cu", "layout.cu", "layout_cluster.cu", "layout_static.cu",
+           "host_pipeline.cu",
            "route_layout.cu",
            "dispatch.cu", "combine.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ep_kernels.cuh", "route_common.cuh",

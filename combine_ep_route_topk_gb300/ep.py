@@ -54,6 +54,16 @@ def lib():
                                   P, P, P]
         L.ep_combine.argtypes = [P, i32, i32, i32, i32, P, P, P, P, ctypes.c_int, i32, P, P]
         L.ep_selftest_wait_timeout.argtypes = [P, P, sz, P]
+        L.ep_host_pipeline_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32,
+                                                      ctypes.c_int, i32]
+        L.ep_host_pipeline_workspace_size.restype = sz
+        L.ep_host_pipeline_create.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.c_int, i32, P,
+                                              P, sz, ctypes.POINTER(P)]
+        L.ep_host_pipeline_step.argtypes = [P, P, P, P, P, P, P]
+        L.ep_host_pipeline_join.argtypes = [P, P]
+        L.ep_host_pipeline_buffer.argtypes = [P, ctypes.c_int, ctypes.POINTER(P),
+                                              ctypes.POINTER(sz)]
+        L.ep_host_pipeline_destroy.argtypes = [P]
         for f in ("ep_route_topk", "ep_expert_balance_map", "ep_dispatch_layout", "ep_dispatch",
                   "ep_combine"):
             getattr(L, f).restype = ctypes.c_int

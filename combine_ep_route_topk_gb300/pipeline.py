@@ -21,11 +21,12 @@ chunked
     HBM-bound dispatch and combine.
 
 HostPipeline
-    Steps whose inputs and result live in pinned host memory.  Copies in,
-    kernels and copies out run on three streams, and the device side of the
-    inputs and the result is double-buffered, so one step's copies in
-    overlap the previous step's kernels and copy out.  The host link, not
-    HBM, bounds such a step.
+    Steps whose inputs and result live in pinned host memory: the binding of
+    the library's native pipeline (ep_host_pipeline_*).  Copies in, kernels
+    and copies out run on three streams, and the device side of the inputs
+    and the result is double-buffered, so one step's copies in overlap the
+    previous step's kernels and copy out.  The host link, not HBM, bounds
+    such a step.
 
 All only call the C ABI through the binding (every step runs in the
 library's kernels); the host work is slicing and stream ordering.
@@ -231,112 +232,116 @@ def chunked(logits, x, rank_offsets_host, K, dtype, bufs, expert_out, comb, ro_r
 
 
 class HostPipeline:
-    """route -> layout -> dispatch -> combine over host buffers, pipelined.
+    """route -> layout -> dispatch -> combine over host buffers, pipelined:
+    the binding of the library's native pipeline (ep_host_pipeline_* in
+    include/ep.h), which owns three streams and the events that order them.
 
     Each `step(x_h, logits_h, rank_offsets_h, y_h, out_h)` enqueues: the
     copies in of the step's logits, rank offsets, tokens x and expert outputs
-    y (pinned host tensors, the shapes of the single-batch path) on the
-    copy-in stream; route and layout once the logits are in, dispatch once x
-    is in, combine once y is in, on the kernel stream; the copy of the
-    combined [N, H] bf16 result to out_h on the copy-out stream.  `depth`
-    device buffer sets rotate, so step i + 1's copies in run under step i's
-    kernels and copy out; a set is reused only after the kernels and the copy
-    out of the step that used it last are done.
+    y (CPU tensors, pinned for the copies to overlap; the shapes of the
+    single-batch path); route and layout once the logits are in, dispatch once
+    x is in, combine once y is in; the copy of the combined [N, H] bf16 result
+    to out_h.  `depth` device buffer sets rotate, so step i + 1's copies in run
+    under step i's kernels and copy out; a set is reused only after the
+    kernels and the copy out of the step that last used it are done.
 
     y holds the expert outputs of the dispatched rows in the step's own
     expert-major order ([N*K, H] contiguous; [E, cap, H] when cap > 0, the
     masked layout), as the caller's expert stage would produce them.
     `expert_map` (device int32 [E], optional) renumbers experts in routing,
-    the same map every step.  The host tensors must stay untouched until the step's
-    copies are done: `synchronize()` (or `join()` and a sync of the calling
-    stream) waits for every step enqueued so far.  After it, `out` (and
-    `scales` for FP8) hold the last step's dispatched rows and `layout` its
-    layout.
+    the same map every step.  The host tensors must stay untouched until the
+    step's copies are done: `synchronize()` (or `join()` and a sync of the
+    calling stream) waits for every step enqueued so far.  After it, `out`
+    (and `scales` for FP8) hold the last step's dispatched rows and `layout`
+    its layout (views into the pipeline's workspace).
     """
 
     def __init__(self, N, E, K, H, R, dtype=_ep.EP_DTYPE_BF16, device="cuda", cap=0,
                  expert_map=None, depth=2):
+        import ctypes
+        L = _ep.lib()
         dev = torch.device(device)
-        self.N, self.E, self.K, self.H, self.R, self.dtype = N, E, K, H, R, dtype
-        self.cap = cap
+        if dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.N, self.E, self.K, self.H, self.R = N, E, K, H, R
+        self.dtype, self.cap, self.depth = dtype, cap, depth
         self.layout_kind = _ep.EP_LAYOUT_MASKED if cap > 0 else _ep.EP_LAYOUT_CONTIG
-        self.expert_map = expert_map
-        rows = _ep.dispatch_rows(N, K, E, self.layout_kind, cap)
+        self.rows = _ep.dispatch_rows(N, K, E, self.layout_kind, cap)
+        size = L.ep_host_pipeline_workspace_size(N, E, K, H, R, cap, dtype, depth)
+        if size == 0:
+            raise _ep.EPError(f"host pipeline: unsupported sizes N={N} E={E} K={K} H={H} "
+                              f"R={R} cap={cap} depth={depth}")
+        self.device = dev
+        self.expert_map = expert_map  # the pipeline reads it on every step
+        emap = None if expert_map is None else _ep._dev(expert_map, torch.int32, "expert_map",
+                                                        (E,))
+        with torch.cuda.device(dev):
+            self.workspace = torch.empty(size, dtype=torch.uint8, device=dev)
+            self._h = ctypes.c_void_p()
+            _ep._check("ep_host_pipeline_create", L.ep_host_pipeline_create(
+                N, E, K, H, R, cap, dtype, depth, emap,
+                ctypes.c_void_p(self.workspace.data_ptr()), size, ctypes.byref(self._h)))
         fp8 = dtype == _ep.EP_DTYPE_FP8_E4M3_B128
-        self.sets = [dict(
-            logits=torch.empty(N, E, dtype=torch.float32, device=dev),
-            ro=torch.empty(R + 1, dtype=torch.int32, device=dev),
-            x=torch.empty(N, H, dtype=torch.bfloat16, device=dev),
-            y=torch.empty(rows, H, dtype=torch.bfloat16, device=dev),
-            comb=torch.empty(N, H, dtype=torch.bfloat16, device=dev)) for _ in range(depth)]
-        self.idx = torch.empty(N, K, dtype=torch.int32, device=dev)
-        self.wt = torch.empty(N, K, dtype=torch.float32, device=dev)
-        self.layout = _ep.alloc_layout(N, E, K, R, cap, dev)
-        self.ws = torch.empty(_ep.ep_dispatch_layout_workspace_size(N, E, K, R),
-                              dtype=torch.uint8, device=dev)
-        self.out = torch.empty(rows, H, dtype=torch.uint8 if fp8 else torch.bfloat16,
-                               device=dev)
-        self.scales = (torch.empty(rows, H // 128, dtype=torch.float32, device=dev)
-                       if fp8 else None)
-        self.h2d = torch.cuda.Stream(device=dev)
-        self.comp = torch.cuda.Stream(device=dev)
-        self.d2h = torch.cuda.Stream(device=dev)
-        self.inputs_free = [None] * depth   # kernels of the set's last step done
-        self.result_free = [None] * depth   # copy out of the set's last step done
-        self.steps = 0
+        self.out = self._view(9, (self.rows, H), torch.uint8 if fp8 else torch.bfloat16)
+        self.scales = self._view(10, (self.rows, H // 128), torch.float32) if fp8 else None
+        self.topk_idx = self._view(0, (N, K), torch.int32)
+        self.topk_w = self._view(1, (N, K), torch.float32)
+        self.layout = _ep.Layout(
+            self._view(2, (R, E), torch.int32), self._view(3, (E + 1,), torch.int32),
+            self._view(4, (R, E), torch.int32), self._view(5, (N, K), torch.int32),
+            self._view(6, (N * K,), torch.int32),
+            self._view(7, (E,), torch.int32) if cap > 0 else None,
+            self._view(8, (1,), torch.int32) if cap > 0 else None)
 
-    def _event(self, stream):
-        ev = torch.cuda.Event()
-        ev.record(stream)
-        return ev
+    def _view(self, which, shape, dtype):
+        """Tensor view of one of the pipeline's device buffers (its workspace)."""
+        import ctypes
+        ptr, nbytes = ctypes.c_void_p(), ctypes.c_size_t()
+        _ep._check("ep_host_pipeline_buffer", _ep.lib().ep_host_pipeline_buffer(
+            self._h, which, ctypes.byref(ptr), ctypes.byref(nbytes)))
+        off = ptr.value - self.workspace.data_ptr()
+        return self.workspace[off:off + nbytes.value].view(dtype).view(shape)
+
+    def _host(self, t, dtype, numel, name):
+        import ctypes
+        if not isinstance(t, torch.Tensor) or t.is_cuda:
+            raise _ep.EPError(f"{name} must be a CPU tensor")
+        if t.dtype != dtype or not t.is_contiguous() or t.numel() != numel:
+            raise _ep.EPError(f"{name} must be a contiguous {dtype} tensor of {numel} elements")
+        return ctypes.c_void_p(t.data_ptr())
 
     def step(self, x_h, logits_h, rank_offsets_h, y_h, out_h):
-        j = self.steps % len(self.sets)
-        b = self.sets[j]
-        if y_h.numel() != b["y"].numel():
-            raise _ep.EPError(f"y must hold {b['y'].shape[0]} x {self.H} elements")
-        caller = torch.cuda.current_stream(b["x"].device)
-        for s in (self.h2d, self.comp, self.d2h):
-            s.wait_stream(caller)
-        if self.inputs_free[j] is not None:
-            self.h2d.wait_event(self.inputs_free[j])
-        with torch.cuda.stream(self.h2d):
-            b["logits"].copy_(logits_h, non_blocking=True)
-            b["ro"].copy_(rank_offsets_h, non_blocking=True)
-            routed_in = self._event(self.h2d)
-            b["x"].copy_(x_h, non_blocking=True)
-            x_in = self._event(self.h2d)
-            b["y"].view(y_h.shape).copy_(y_h, non_blocking=True)
-            y_in = self._event(self.h2d)
-        E, K = self.E, self.K
-        with torch.cuda.stream(self.comp):
-            self.comp.wait_event(routed_in)
-            _ep.ep_route_topk(b["logits"], K, expert_map=self.expert_map, topk_idx=self.idx,
-                              topk_w=self.wt)
-            lay = _ep.ep_dispatch_layout(self.idx, b["ro"], E, self.cap, out=self.layout,
-                                         workspace=self.ws)
-            self.comp.wait_event(x_in)
-            _ep.ep_dispatch(b["x"], self.idx, lay.pos, lay.expert_offsets, E,
-                            self.layout_kind, self.cap, self.dtype, out=self.out,
-                            out_scales=self.scales)
-            self.comp.wait_event(y_in)
-            if self.result_free[j] is not None:
-                self.comp.wait_event(self.result_free[j])
-            _ep.ep_combine(b["y"], self.idx, self.wt, lay.pos, lay.expert_offsets, E,
-                           self.layout_kind, self.cap, out=b["comb"])
-            self.inputs_free[j] = self._event(self.comp)
-        with torch.cuda.stream(self.d2h):
-            self.d2h.wait_event(self.inputs_free[j])
-            out_h.copy_(b["comb"], non_blocking=True)
-            self.result_free[j] = self._event(self.d2h)
-        self.steps += 1
+        N, E, K, H, R = self.N, self.E, self.K, self.H, self.R
+        args = (self._host(logits_h, torch.float32, N * E, "logits_h"),
+                self._host(rank_offsets_h, torch.int32, R + 1, "rank_offsets_h"),
+                self._host(x_h, torch.bfloat16, N * H, "x_h"),
+                self._host(y_h, torch.bfloat16, self.rows * H, "y_h"),
+                self._host(out_h, torch.bfloat16, N * H, "out_h"))
+        with torch.cuda.device(self.device):
+            _ep._check("ep_host_pipeline_step", _ep.lib().ep_host_pipeline_step(
+                self._h, *args, _ep._stream(None)))
 
     def join(self, stream=None):
         """Make `stream` (default: the current one) wait for every step."""
-        s = torch.cuda.current_stream(self.idx.device) if stream is None else stream
-        for t in (self.h2d, self.comp, self.d2h):
-            s.wait_stream(t)
+        with torch.cuda.device(self.device):
+            _ep._check("ep_host_pipeline_join",
+                       _ep.lib().ep_host_pipeline_join(self._h, _ep._stream(stream)))
 
     def synchronize(self):
-        for t in (self.h2d, self.comp, self.d2h):
-            t.synchronize()
+        with torch.cuda.device(self.device):
+            s = torch.cuda.current_stream()
+            self.join(s)
+            s.synchronize()
+
+    def close(self):
+        """Wait for the pipeline and release its streams and events."""
+        h, self._h = getattr(self, "_h", None), None
+        if h is not None and h.value:
+            with torch.cuda.device(self.device):
+                _ep._check("ep_host_pipeline_destroy", _ep.lib().ep_host_pipeline_destroy(h))
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown: the library may be gone
+            pass

@@ -264,6 +264,83 @@ ep_status_t ep_combine(const void* y, int32_t N, int32_t H, int32_t E, int32_t K
                        void* out, void* stream);
 
 /*
+ * ep_host_pipeline_* -- no counterpart in the source pages: the path for
+ * callers whose inputs and results live in host memory.  Each step copies the
+ * step's logits, rank offsets, tokens x and expert outputs y in, runs
+ * ep_route_topk, ep_dispatch_layout, ep_dispatch and ep_combine, and copies
+ * the combined [N, H] bf16 result out.  Copies in, kernels and the copy out
+ * run on three streams of the pipeline.  `depth` device buffer sets rotate,
+ * so a step's copies in overlap the previous step's kernels and copy out.
+ * A set is reused only after the kernels and the copy out of the step that
+ * last used it are done.
+ *   N, E, K, H, R, cap, dtype  as for the four calls (cap > 0: masked layout,
+ *              y is [E, cap, H]; cap == 0: contiguous, y is [N*K, H]);
+ *              N >= 1; depth 1..4 (1: each step waits for the previous).
+ *   expert_map device int32 [E] or NULL, the same for every step; it must
+ *              stay valid while the pipeline exists.
+ *   workspace  device memory of at least ep_host_pipeline_workspace_size
+ *              bytes, 256-byte aligned, owned by the caller and kept alive
+ *              (and untouched) until ep_host_pipeline_destroy returns.  Every
+ *              device buffer of the pipeline lives in it.
+ * The object itself holds three streams and 5*depth + 1 events on the device
+ * that was current at creation; call its functions with that device
+ * current.
+ */
+typedef struct ep_host_pipeline ep_host_pipeline_t;
+
+/* Bytes of workspace a pipeline needs; 0 for invalid or unsupported sizes. */
+size_t ep_host_pipeline_workspace_size(int32_t N, int32_t E, int32_t K, int32_t H, int32_t R,
+                                       int32_t cap, ep_dtype_t dtype, int32_t depth);
+
+/* Creates a pipeline in *out.  EP_ERR_INVALID_ARG / EP_ERR_UNSUPPORTED for
+ * sizes outside the four calls' limits (or depth outside 1..4),
+ * EP_ERR_WORKSPACE for a missing, small or misaligned workspace, EP_ERR_CUDA
+ * if a stream or event cannot be created (*out is then NULL). */
+ep_status_t ep_host_pipeline_create(int32_t N, int32_t E, int32_t K, int32_t H, int32_t R,
+                                    int32_t cap, ep_dtype_t dtype, int32_t depth,
+                                    const int32_t* expert_map, void* workspace, size_t ws_bytes,
+                                    ep_host_pipeline_t** out);
+
+/* Enqueues one step.  Host buffers (page-locked for the copies to overlap;
+ * pageable memory works but its copies do not overlap): logits_h float32
+ * [N, E], rank_offsets_h int32 [R+1], x_h bf16 [N, H], y_h bf16 [N*K, H] or
+ * [E, cap, H], out_h bf16 [N, H].  The step starts after the work enqueued
+ * on `stream` before the call.  The inputs must stay untouched and out_h
+ * unread until the step is done (ep_host_pipeline_join, then a sync of
+ * `stream`).  An argument or launch failure returns its status; the
+ * pipeline's streams may then hold part of the step. */
+ep_status_t ep_host_pipeline_step(ep_host_pipeline_t* pipeline, const float* logits_h,
+                                  const int32_t* rank_offsets_h, const void* x_h,
+                                  const void* y_h, void* out_h, void* stream);
+
+/* Makes `stream` wait for every step enqueued so far. */
+ep_status_t ep_host_pipeline_join(ep_host_pipeline_t* pipeline, void* stream);
+
+/* Device buffers of the last step's intermediate outputs, inside the
+ * workspace (valid after a join and a sync): the routed picks and weights,
+ * the layout, and the dispatched rows (and FP8 scales). */
+typedef enum {
+    EP_HOST_BUF_TOPK_IDX = 0,
+    EP_HOST_BUF_TOPK_W = 1,
+    EP_HOST_BUF_COUNTS = 2,
+    EP_HOST_BUF_EXPERT_OFFSETS = 3,
+    EP_HOST_BUF_RANK_EXPERT_OFFSETS = 4,
+    EP_HOST_BUF_POS = 5,
+    EP_HOST_BUF_ROW_SRC = 6,
+    EP_HOST_BUF_MASKED_M = 7,      /* 0 bytes when cap == 0 */
+    EP_HOST_BUF_OVERFLOW = 8,      /* 0 bytes when cap == 0 */
+    EP_HOST_BUF_OUT = 9,
+    EP_HOST_BUF_OUT_SCALES = 10    /* 0 bytes for bf16 */
+} ep_host_buffer_t;
+
+ep_status_t ep_host_pipeline_buffer(const ep_host_pipeline_t* pipeline, ep_host_buffer_t which,
+                                    void** device_ptr, size_t* bytes);
+
+/* Waits for the pipeline's streams, then releases its streams and events and
+ * the object (NULL is a no-op).  The workspace is the caller's to free. */
+ep_status_t ep_host_pipeline_destroy(ep_host_pipeline_t* pipeline);
+
+/*
  * ep_selftest_wait_timeout -- no counterpart in the source pages: a check of
  * the bounded wait that guards the grid barriers of ep_route_layout.  It
  * launches a 2-block kernel whose barrier waits for a third block that never

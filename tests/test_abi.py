@@ -116,6 +116,37 @@ def test_binding_refuses_cpu_tensors(L):
                          topk_w=torch.zeros(4, 2))
 
 
+def test_host_pipeline_argument_checks(L):
+    size = L.ep_host_pipeline_workspace_size
+    assert size(1024, 256, 8, 7168, 8, 128, 0, 2) > 0
+    assert size(1024, 256, 8, 7168, 8, 128, 0, 2) < size(1024, 256, 8, 7168, 8, 128, 0, 3)
+    assert size(0, 256, 8, 7168, 8, 0, 0, 2) == 0          # N >= 1
+    assert size(10, 16, 2, 100, 4, 0, 0, 2) == 0           # H % 8
+    assert size(10, 16, 2, 200, 4, 0, 1, 2) == 0           # FP8 needs H % 128
+    assert size(10, 16, 2, 128, 4, 0, 0, 5) == 0           # depth 1..4
+    create = L.ep_host_pipeline_create
+    need = size(10, 16, 2, 128, 4, 0, 0, 2)
+    out = P()
+    assert create(10, 16, 2, 128, 4, 0, 0, 2, None, p(4096), need, None) == INVALID  # no out
+    assert create(10, 16, 17, 128, 4, 0, 0, 2, None, p(4096), need,
+                  ctypes.byref(out)) == INVALID                                  # K > E
+    assert create(10, 2048, 2, 128, 4, 0, 0, 2, None, p(4096), need,
+                  ctypes.byref(out)) == UNSUPPORTED                              # E > 1024
+    assert create(10, 16, 2, 128, 4, 0, 0, 2, None, p(4096), need - 1,
+                  ctypes.byref(out)) == WORKSPACE
+    assert create(10, 16, 2, 128, 4, 0, 0, 2, None, p(4096 + 16), need,
+                  ctypes.byref(out)) == WORKSPACE                                # 256-byte aligned
+    assert create(10, 16, 2, 128, 4, 0, 0, 2, p(4098), p(4096), need,
+                  ctypes.byref(out)) == INVALID                                  # expert_map align
+    assert out.value is None
+    assert L.ep_host_pipeline_step(None, p(), p(), p(), p(), p(), None) == INVALID
+    assert L.ep_host_pipeline_join(None, None) == INVALID
+    ptr, nb = P(), ctypes.c_size_t()
+    assert L.ep_host_pipeline_buffer(None, 0, ctypes.byref(ptr), ctypes.byref(nb)) == INVALID
+    assert L.ep_host_pipeline_destroy(None) == OK
+    assert L.ep_kernel_launch_count() == 0
+
+
 C_CLIENT = r"""
 #include <stdio.h>
 #include "ep.h"
