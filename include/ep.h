@@ -28,11 +28,14 @@
  *
  * Conventions for every entry point:
  *   - Pointers are device pointers owned by the caller unless stated; the
- *     library allocates and frees nothing, and keeps no pointer after return.
+ *     library allocates and frees no device memory, and keeps no pointer
+ *     after return (except a host pipeline, which keeps its workspace and
+ *     expert map, and holds streams and events until destroyed).
  *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is
- *     the legacy default stream) and returns without synchronising; no call
- *     reads device memory on the host, so every call can be captured in a
- *     CUDA graph.
+ *     the legacy default stream) and returns without synchronising
+ *     (ep_host_pipeline_destroy alone waits, for its own streams); no call
+ *     reads device memory on the host, so the four calls and the layout
+ *     variants can be captured in a CUDA graph.
  *   - Arguments are checked on the host before anything is launched; a bad
  *     argument returns EP_ERR_INVALID_ARG (or EP_ERR_WORKSPACE /
  *     EP_ERR_UNSUPPORTED) and launches nothing.  A failed launch returns
