@@ -313,8 +313,8 @@ def run_ours(args, world, rank, local):
         # Host-link bandwidth is shared with the machine's other users and drifts,
         # so the two schedules alternate in windows and each reports its median
         # window.
-        n_win = 3
-        e2e_steps = max(2, min(args.steps, 24) // n_win)  # steps per window
+        n_win = 5
+        e2e_steps = max(2, min(args.steps, 30) // n_win)  # steps per window
         def pinned_copy(t):
             h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
             h.copy_(t)
