@@ -3,10 +3,11 @@
 // ("Anatomy of a High-Performance EP Kernel": route locally, then "ask first,
 // then send"), without the launches and ramp-ups in between.
 //
-//   phase 1  each block takes chunks of C tokens (chunks never straddle a
-//            rank); each warp routes tokens of the chunk (route::route_token)
-//            and the block counts the chunk's picks per expert in shared
-//            memory, then writes the chunk histogram row.
+//   phase 1  tokens go round-robin to every warp of the grid (balanced to
+//            one token per warp); each warp routes its tokens
+//            (route::route_token) and adds each pick to its chunk's
+//            histogram row with an L2 atomic (chunks of C tokens never
+//            straddle a rank; the rows are zeroed before the launch).
 //   barrier
 //   phase 2  blocks take tiles of 32 expert columns; each warp scans a group
 //            of chunk rows (coalesced 128-byte reads) and the block combines
@@ -21,6 +22,8 @@
 // counter in the workspace, zeroed by a memset before the launch; each wait
 // is bounded (kSpinLimit polls with a back-off) and, if it ever ran out, the
 // block would record 1 in `status` and return instead of waiting on.
+#include <algorithm>
+
 #include "ep.h"
 #include "ep_kernels.cuh"
 #include "layout_common.cuh"
@@ -29,8 +32,11 @@
 namespace ep {
 
 int route_layout_chunk_tokens(int N) {
-    int C = (N + 1023) / 1024;  // up to ~1024 chunks: routing wants many warps
-    C = ((C + 7) / 8) * 8;      // 8 tokens = one per warp of a block
+    // About 256 chunks, as in the layout kernels: routing goes round-robin over
+    // all warps whatever the chunk size, and fewer chunk rows keep the column
+    // scans short.
+    int C = (N + 255) / 256;
+    C = ((C + 7) / 8) * 8;
     return C < 8 ? 8 : C;
 }
 
@@ -102,6 +108,18 @@ __global__ void __launch_bounds__(32) barrier_timeout_kernel(unsigned* ctr, unsi
     grid_barrier(ctr, gridDim.x + 1, limit, status);
 }
 
+// Rank of token t, s_m[0] <= t < s_m[R]: the r with s_m[r] <= t < s_m[r+1]
+// (s_m non-decreasing; empty ranks never match).
+__device__ __forceinline__ int token_rank(const int* s_m, int R, int t) {
+    int lo = 0, hi = R - 1;
+    while (lo < hi) {  // largest r < R with s_m[r] <= t
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_m[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
 template <int VPL, bool VEC, int KT>
 __global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
     extern __shared__ int smem[];
@@ -117,28 +135,24 @@ __global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
     const int K = KT > 0 ? KT : a.K;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-    // ---- phase 1: route the chunk's tokens, count its picks per expert
-    for (int c = blockIdx.x; c < S; c += gridDim.x) {
-        for (int e = threadIdx.x; e < E; e += kNT) s_w[e] = 0;
-        __syncthreads();
-        const int r = chunk_rank(s_tab, a.R, c);
-        const int tok0 = s_m[r] + (c - s_tab[r]) * C;
-        const int tok1 = min(tok0 + C, s_m[r + 1]);
-        for (int t = tok0 + warp; t < tok1; t += kWarps) {
-            int id;
-            float w;
-            route::route_token<VPL, VEC, KT>(f.logits + (size_t)t * E, E, a.K, f.emap, lane, id,
-                                             w);
-            if (lane < K) {
-                f.topk_idx[(size_t)t * K + lane] = id;
-                f.topk_w[(size_t)t * K + lane] = w;
-                if (id >= 0) atomicAdd(&s_w[id], 1);
+    // ---- phase 1: tokens round-robin over every warp of the grid (balanced
+    // to one token); each pick counts into its chunk's histogram row, zeroed
+    // before the launch, with an L2 atomic
+    const int gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
+    const int t_lo = s_m[0], t_hi = s_m[a.R];  // tokens that belong to a rank
+    for (int t = gw; t < a.N; t += nw) {
+        int id;
+        float w;
+        route::route_token<VPL, VEC, KT>(f.logits + (size_t)t * E, E, a.K, f.emap, lane, id, w);
+        if (lane < K) {
+            f.topk_idx[(size_t)t * K + lane] = id;
+            f.topk_w[(size_t)t * K + lane] = w;
+            if (id >= 0 && t >= t_lo && t < t_hi) {
+                const int r = token_rank(s_m, a.R, t);
+                const int c = s_tab[r] + (t - s_m[r]) / C;
+                atomicAdd(a.ws_hist + (size_t)c * E + id, 1);
             }
         }
-        __syncthreads();
-        int* row = a.ws_hist + (size_t)c * E;
-        for (int e = threadIdx.x; e < E; e += kNT) row[e] = s_w[e];
-        __syncthreads();
     }
     if (!grid_barrier(f.bar + 0, gridDim.x, kSpinLimit, f.status)) return;
 
@@ -150,9 +164,17 @@ __global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
         const bool live = e < E;
         const int rpg = (S + kWarps - 1) / kWarps;
         const int r0 = min(S, warp * rpg), r1 = min(S, r0 + rpg);
+        constexpr int kB = 8;  // rows whose loads are in flight together
         int sum = 0;
         if (live)
-            for (int c = r0; c < r1; ++c) sum += __ldcg(hist + (size_t)c * E + e);
+            for (int c0 = r0; c0 < r1; c0 += kB) {
+                int v[kB];
+#pragma unroll
+                for (int b = 0; b < kB; ++b)
+                    v[b] = (c0 + b < r1) ? __ldcg(hist + (size_t)(c0 + b) * E + e) : 0;
+#pragma unroll
+                for (int b = 0; b < kB; ++b) sum += v[b];
+            }
         s_w[warp * 32 + lane] = sum;
         __syncthreads();
         int run = 0, total = 0;
@@ -162,11 +184,17 @@ __global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
             total += v;
         }
         if (live)
-            for (int c = r0; c < r1; ++c) {
-                const size_t at = (size_t)c * E + e;
-                const int v = __ldcg(hist + at);
-                hist[at] = run;
-                run += v;
+            for (int c0 = r0; c0 < r1; c0 += kB) {
+                int v[kB];
+#pragma unroll
+                for (int b = 0; b < kB; ++b)
+                    v[b] = (c0 + b < r1) ? __ldcg(hist + (size_t)(c0 + b) * E + e) : 0;
+#pragma unroll
+                for (int b = 0; b < kB; ++b)
+                    if (c0 + b < r1) {
+                        hist[(size_t)(c0 + b) * E + e] = run;
+                        run += v[b];
+                    }
             }
         if (warp == 0) {
             s_w[kWarps * 32 + lane] = total;
@@ -198,13 +226,18 @@ __global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
 template <int VPL, bool VEC, int KT>
 cudaError_t launch_fused_t(FusedArgs& f, int C, int slots, size_t smem, cudaStream_t s,
                            bool* launched) {
+    const int N = f.a.N;
     auto* fn = route_layout_kernel<VPL, VEC, KT>;
     int per_sm = 0;
     cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kNT, smem);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaSuccess;  // not launched: caller falls back
-    int grid = per_sm * sm_count();
-    if (grid > slots) grid = slots;
+    // Enough blocks for about 4 tokens per warp in phase 1 and one block per
+    // chunk in phase 3, but no more (a larger grid only slows the barriers
+    // and repeats the per-block offset work), and never more than can be
+    // resident at once.
+    const int want = std::max(slots, (N + kWarps * 4 - 1) / (kWarps * 4));
+    int grid = std::min(per_sm * sm_count(), want);
     if (grid < 1) grid = 1;
     void* args[] = {&f, &C};
     err = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fn), dim3(grid), dim3(kNT),
@@ -247,6 +280,9 @@ cudaError_t launch_route_layout(const RouteLayoutArgs& r, cudaStream_t s, bool* 
                                  kWarps * (a.E > kNT ? a.E : kNT)) * sizeof(int);
     cudaError_t err = cudaMemsetAsync(f.bar, 0, 2 * sizeof(unsigned), s);
     if (err == cudaSuccess && r.status) err = cudaMemsetAsync(r.status, 0, sizeof(int32_t), s);
+    // phase 1 counts into the chunk histograms with atomics
+    if (err == cudaSuccess)
+        err = cudaMemsetAsync(f.a.ws_hist, 0, (size_t)slots * a.E * sizeof(int32_t), s);
     if (err != cudaSuccess) return err;
     const int K = a.K;
     if (vec && a.E == 256) {
