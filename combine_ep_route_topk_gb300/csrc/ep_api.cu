@@ -194,6 +194,8 @@ ep_status_t ep_route_layout(const float* logits, const int32_t* rank_offsets, in
     if (err != cudaSuccess) return cuda_status(err);
     if (launched) return EP_OK;
     // no fused instance for these sizes: the same results from the two kernels
+    if (status) err = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
+    if (err != cudaSuccess) return cuda_status(err);
     err = launch_route_topk(logits, N, E, K, expert_map, topk_idx, topk_w, s);
     if (err != cudaSuccess) return cuda_status(err);
     a.ws_hist = static_cast<int32_t*>(workspace);

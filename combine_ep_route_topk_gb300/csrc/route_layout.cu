@@ -19,9 +19,10 @@
 //
 // The grid never exceeds the blocks that can be resident at once (the launch
 // is cooperative), so every block reaches each barrier.  A barrier is a
-// counter in the workspace, zeroed by a memset before the launch; each wait
-// is bounded (kSpinLimit polls with a back-off) and, if it ever ran out, the
-// block would record 1 in `status` and return instead of waiting on.
+// counter in the workspace, zeroed (with the chunk histograms) by one memset
+// before the launch; each wait is bounded (kSpinLimit polls with a back-off)
+// and, if it ever ran out, the block would record 1 in `status` and return
+// instead of waiting on.  Block 0 records 0 once both barriers are passed.
 #include <algorithm>
 
 #include "ep.h"
@@ -215,6 +216,8 @@ __global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
         __syncthreads();
     }
     if (!grid_barrier(f.bar + 1, gridDim.x, kSpinLimit, f.status)) return;
+    // every block passed both barriers, so no wait can run out any more
+    if (blockIdx.x == 0 && threadIdx.x == 0 && f.status) *f.status = 0;
 
     // ---- phase 3: offsets, side outputs, stable positions
     load_expert_offsets<kNT>(a.ws_totals, E, s_eoff, s_tmp);
@@ -265,24 +268,25 @@ cudaError_t launch_route_layout(const RouteLayoutArgs& r, cudaStream_t s, bool* 
     const LayoutArgs& a = r.lay;
     const int C = route_layout_chunk_tokens(a.N);
     const int slots = route_layout_chunk_slots(a.N, a.R);
+    // workspace: chunk histograms [slots][E], barrier counters (64 ints, so
+    // one memset zeroes both), expert totals [E]
     FusedArgs f;
     f.a = a;
     f.a.ws_hist = r.workspace;
-    f.a.ws_totals = r.workspace + (size_t)slots * a.E;
+    f.bar = reinterpret_cast<unsigned*>(r.workspace + (size_t)slots * a.E);
+    f.a.ws_totals = r.workspace + (size_t)slots * a.E + 64;
     f.logits = r.logits;
     f.emap = r.emap;
     f.topk_idx = r.topk_idx;
     f.topk_w = r.topk_w;
-    f.bar = reinterpret_cast<unsigned*>(f.a.ws_totals + a.E);
     f.status = r.status;
     const bool vec = (a.E % 128 == 0) && ((reinterpret_cast<uintptr_t>(r.logits) & 15u) == 0);
     const size_t smem = (size_t)(2 * ((a.R + 1 + 3) & ~3) + 32 + ((a.E + 1 + 3) & ~3) +
                                  kWarps * (a.E > kNT ? a.E : kNT)) * sizeof(int);
-    cudaError_t err = cudaMemsetAsync(f.bar, 0, 2 * sizeof(unsigned), s);
-    if (err == cudaSuccess && r.status) err = cudaMemsetAsync(r.status, 0, sizeof(int32_t), s);
-    // phase 1 counts into the chunk histograms with atomics
-    if (err == cudaSuccess)
-        err = cudaMemsetAsync(f.a.ws_hist, 0, (size_t)slots * a.E * sizeof(int32_t), s);
+    // phase 1 counts into the chunk histograms with atomics; the status word
+    // is written by the kernel (0 once both barriers passed, 1 on a timeout)
+    const cudaError_t err =
+        cudaMemsetAsync(r.workspace, 0, ((size_t)slots * a.E + 64) * sizeof(int32_t), s);
     if (err != cudaSuccess) return err;
     const int K = a.K;
     if (vec && a.E == 256) {

@@ -180,9 +180,9 @@ size_t ep_route_layout_workspace_size(int32_t N, int32_t E, int32_t K, int32_t R
  *   workspace ep_route_layout_workspace_size bytes, no initialisation needed.
  * Sizes without a fused instance (E not a multiple of 128 above 256 experts)
  * or a device that cannot hold one block run the two kernels instead, with
- * the same results.  Launches three memsets before the kernel: barrier
- * counters, status, and the chunk histograms that the routing phase counts
- * into.
+ * the same results.  Launches one memset before the kernel (the chunk
+ * histograms that the routing phase counts into, and the barrier counters);
+ * the kernel writes the status word.
  */
 ep_status_t ep_route_layout(const float* logits, const int32_t* rank_offsets, int32_t R,
                             int32_t N, int32_t E, int32_t K, const int32_t* expert_map,
