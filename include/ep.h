@@ -46,9 +46,11 @@
  *     [0,E), rank_offsets that are not a non-decreasing 0..N sequence, pos
  *     values that do not come from ep_dispatch_layout) never cause an access
  *     outside the buffers described here: such picks are skipped.
- *   - Kernels are launched with programmatic dependent launch: each one waits
- *     for the preceding grids of the stream to complete (griddepcontrol.wait)
- *     before touching memory, then lets the next kernel launch early.  A
+ *   - Kernels are launched with programmatic dependent launch (all but the
+ *     cooperative kernel of ep_route_layout, which is a plain cooperative
+ *     launch): each one waits for the preceding grids of the stream to
+ *     complete (griddepcontrol.wait) before touching memory, then lets the
+ *     next kernel launch early.  A
  *     caller kernel that follows ours and is itself launched with the
  *     programmatic-serialisation attribute must wait for its grid dependency
  *     (cudaGridDependencySynchronize) before reading our outputs; kernels
