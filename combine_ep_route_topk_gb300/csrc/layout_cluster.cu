@@ -3,7 +3,7 @@
 // "Dispatch" (the counts and every row position, before any row moves).
 //
 // The same stable counting sort as the three layout kernels, run by one
-// thread-block cluster of kCS CTAs with a single cluster barrier.  Chunks of
+// thread-block cluster of kCS CTAs with one full cluster barrier.  Chunks of
 // C tokens (never straddling a rank) are owned Q per CTA, at most about one
 // per warp:
 //   1. each warp builds its chunk's expert histogram in shared memory (one
@@ -13,14 +13,16 @@
 //      column totals, then pushes through distributed shared memory
 //      (a) its column totals to every CTA and (b) the local prefix row at
 //      every rank boundary it owns to the CTA that writes that rank's counts;
-//   3. cluster barrier: the only one.  Every later read is local;
+//   3. a full cluster barrier.  (An earlier, split one -- arrival at kernel
+//      entry, wait just before the first push -- makes sure that no push
+//      reaches a CTA that has not started.)  Every later read is local;
 //   4. each CTA derives the base of its rows (the totals of earlier CTAs),
 //      the expert totals and offsets, writes the counts and rank offsets of
 //      its ranks (r = j mod kCS) and gives its chunks' picks their positions
 //      in (t, k) order.
 // No CTA touches another's shared memory after the barrier, so each may leave
-// when done.  Every thread of every CTA reaches the barrier, whatever the
-// sizes (no return before it).
+// when done.  Every thread of every CTA reaches both barriers, whatever the
+// sizes (no return before them).
 #include <cooperative_groups.h>
 
 #include <cstdlib>
@@ -128,6 +130,10 @@ __device__ __forceinline__ void scatter_passes(const LayoutArgs& a, int* run, co
 
 __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kCT)
     layout_cluster_kernel(LayoutArgs a, int C, int Q, int RS) {
+    // Announce this CTA to the cluster at once (no memory ordering needed):
+    // the matching wait below, before the first store into another CTA's
+    // shared memory, guarantees that every CTA of the cluster is running.
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     pdl_prologue();
     cg::cluster_group cl = cg::this_cluster();
     const int j = (int)cl.block_rank();
@@ -171,7 +177,11 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kCT)
 
     // 2. local exclusive prefixes down this CTA's rows, column totals to
     //    every CTA, and the prefix rows at the rank boundaries this CTA owns
-    //    to the CTAs that write those ranks
+    //    to the CTAs that write those ranks.  First wait until every CTA of
+    //    the cluster has arrived at the entry barrier, i.e. is running and
+    //    owns its shared memory (the pushed arrays are not touched locally
+    //    before the cluster barrier below, so a running target is enough).
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     for (int e = threadIdx.x; e < E; e += kCT) {
         int run = 0;
         for (int q = 0; q < Q; ++q) {
@@ -196,7 +206,7 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kCT)
             for (int e = lane; e < E; e += 32) dst[e] = s_hist[(size_t)(hi - cq0) * E + e];
         }
     }
-    cl.sync();  // the only cluster barrier: every later access is local
+    cl.sync();  // the one full cluster barrier: every later access is local
 
     // 3. bases, totals and expert offsets
     for (int e = threadIdx.x; e < E; e += kCT) {

@@ -22,7 +22,8 @@
 // counter in the workspace, zeroed (with the chunk histograms) by one memset
 // before the launch; each wait is bounded (kSpinLimit polls with a back-off)
 // and, if it ever ran out, the block would record 1 in `status` and return
-// instead of waiting on.  Block 0 records 0 once both barriers are passed.
+// instead of waiting on.  Block 0 stores 0 in `status` before it arrives at
+// the first barrier, so a 1 recorded by any timeout is never overwritten.
 #include <algorithm>
 
 #include "ep.h"
@@ -155,6 +156,13 @@ __global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
             }
         }
     }
+    // Block 0 clears the status word before it arrives at the first barrier.
+    // Any timeout is recorded after this store: one at the second barrier
+    // comes from a block that passed the first, hence after block 0 arrived
+    // (the barrier's fence and acquire order the two); one at the first
+    // barrier keeps its block from ever arriving at the second, so block 0's
+    // own wait there runs out and records 1 after its 0.
+    if (blockIdx.x == 0 && threadIdx.x == 0 && f.status) *f.status = 0;
     if (!grid_barrier(f.bar + 0, gridDim.x, kSpinLimit, f.status)) return;
 
     // ---- phase 2: tiles of 32 expert columns; warp w scans row group w, so
@@ -216,8 +224,6 @@ __global__ void __launch_bounds__(kNT) route_layout_kernel(FusedArgs f, int C) {
         __syncthreads();
     }
     if (!grid_barrier(f.bar + 1, gridDim.x, kSpinLimit, f.status)) return;
-    // every block passed both barriers, so no wait can run out any more
-    if (blockIdx.x == 0 && threadIdx.x == 0 && f.status) *f.status = 0;
 
     // ---- phase 3: offsets, side outputs, stable positions
     load_expert_offsets<kNT>(a.ws_totals, E, s_eoff, s_tmp);
@@ -284,7 +290,8 @@ cudaError_t launch_route_layout(const RouteLayoutArgs& r, cudaStream_t s, bool* 
     const size_t smem = (size_t)(2 * ((a.R + 1 + 3) & ~3) + 32 + ((a.E + 1 + 3) & ~3) +
                                  kWarps * (a.E > kNT ? a.E : kNT)) * sizeof(int);
     // phase 1 counts into the chunk histograms with atomics; the status word
-    // is written by the kernel (0 once both barriers passed, 1 on a timeout)
+    // is written by the kernel (0 by block 0 before the first barrier, 1 by
+    // any block whose wait runs out)
     const cudaError_t err =
         cudaMemsetAsync(r.workspace, 0, ((size_t)slots * a.E + 64) * sizeof(int32_t), s);
     if (err != cudaSuccess) return err;

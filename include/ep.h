@@ -155,6 +155,12 @@ size_t ep_dispatch_layout_workspace_size(int32_t N, int32_t E, int32_t K, int32_
  *                       cap, which the masked layout drops.
  *   workspace           device scratch of ws_bytes >= the size above; its
  *                       contents need no initialisation and are clobbered.
+ * R need not divide E.  The layout uses a rank only as a range of tokens
+ * (its counts row and where its rows start in each expert segment); which
+ * experts a rank hosts (E/R contiguous ones, [Moreh] "Parallelization
+ * method") matters only to ep_expert_balance_map, which requires E % R == 0.
+ * A micro-batch of a subset of the ranks (one rank of eight, say, with all
+ * 256 experts) is therefore a valid layout problem.
  * Problems of at most 16384 picks (N*K) and 64 ranks whose chunk rows fit in
  * shared memory run as one launch of one thread-block cluster; larger ones as
  * three kernels.  EP_LAYOUT_CLUSTER=0 in the environment (read at every call)
@@ -179,6 +185,10 @@ size_t ep_route_layout_workspace_size(int32_t N, int32_t E, int32_t K, int32_t R
  *   status    int32 [1] device, or NULL: 0 when the call completed, 1 if a
  *             block's bounded wait at an internal grid barrier ran out
  *             (results then incomplete; the co-resident launch rules it out).
+ *             Written on every call (need not be cleared): the kernel stores
+ *             0 before its first barrier and any timeout stores 1 after
+ *             that, so a 1 is never overwritten; the two-kernel fallback
+ *             clears it with a memset.
  *   workspace ep_route_layout_workspace_size bytes, no initialisation needed.
  * Sizes without a fused instance (E not a multiple of 128 above 256 experts)
  * or a device that cannot hold one block run the two kernels instead, with
@@ -211,7 +221,12 @@ ep_status_t ep_route_layout(const float* logits, const int32_t* rank_offsets, in
  *     nothing; other argument errors as for ep_dispatch_layout.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
- *     stream capture.  A failed lookup returns EP_ERR_CUDA.
+ *     stream capture.  A failed lookup returns EP_ERR_CUDA.  The cached
+ *     address belongs to the device's current context: after
+ *     cudaDeviceReset (or anything else that destroys and recreates the
+ *     primary context) the library reloads and the array may move, so do
+ *     not call this entry point again in a process that has reset a device
+ *     it was used on.
  *   - Allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
  *   - All calls share the array and it keeps the last call's contents; the
  *     kernels write every entry they read, so nothing needs clearing.  Calls
