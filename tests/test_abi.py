@@ -187,3 +187,16 @@ def test_header_is_plain_c_and_the_library_links_from_c(L, tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, (r.returncode, r.stderr)
     assert r.stdout.strip() == "EP_ERR_UNSUPPORTED"
+
+
+def test_host_memory_argument_checks(L):
+    """ep_host_alloc / ep_host_free / ep_host_pipeline_copy_ms refuse bad
+    arguments on the host, before any mapping or CUDA call."""
+    out = P(1234)
+    assert L.ep_host_alloc(0, ctypes.byref(out)) == INVALID
+    assert out.value is None  # cleared on failure
+    assert L.ep_host_alloc(4096, None) == INVALID
+    assert L.ep_host_free(None) == OK
+    assert L.ep_host_free(p(4096)) == INVALID  # not from ep_host_alloc
+    a, b = ctypes.c_float(), ctypes.c_float()
+    assert L.ep_host_pipeline_copy_ms(None, ctypes.byref(a), ctypes.byref(b)) == INVALID

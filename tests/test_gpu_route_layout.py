@@ -119,3 +119,28 @@ def test_bounded_wait_gives_up_and_the_context_stays_usable():
     idx, w = ep.ep_route_topk(logits.cuda(), 4)
     ref_idx, _ = oracle.route_topk(logits.numpy(), 4)
     np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+
+
+@pytest.mark.parametrize("E", [256, 384])  # a fused instance; the two-kernel fallback
+def test_status_word_left_at_one_is_cleared_by_the_next_call(E):
+    """The status word is written on every call: a 1 left in it (here by the
+    bounded-wait self-test, which records a timeout into the same word) reads
+    0 after a normal call, on the fused kernel and on the two-kernel fallback
+    (E = 384 has no fused instance), and the results match the oracle."""
+    status = ep.ep_selftest_wait_timeout()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    g = torch.Generator().manual_seed(E)
+    B = [120, 0, 77, 300]
+    N, K = sum(B), 8
+    offs = np.concatenate([[0], np.cumsum(B)]).astype(np.int32)
+    logits = torch.randn(N, E, generator=g)
+    idx, w, lay = ep.ep_route_layout(logits.cuda(), torch.from_numpy(offs).cuda(), K, 0,
+                                     status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ridx, _ = oracle.route_topk(logits.numpy(), K)
+    ref = oracle.layout(ridx, offs, E)
+    np.testing.assert_array_equal(np_(idx), ridx)
+    for name in ("counts", "expert_offsets", "rank_expert_offsets", "pos", "row_src"):
+        np.testing.assert_array_equal(np_(getattr(lay, name)), ref[name], err_msg=name)
