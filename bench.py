@@ -198,7 +198,7 @@ def run_ours(args, world, rank, local):
     import torch
     import combine_ep_route_topk_gb300 as ep
     from combine_ep_route_topk_gb300 import workloads as wl
-    from combine_ep_route_topk_gb300.pipeline import HostPipeline
+    from combine_ep_route_topk_gb300.pipeline import HostPipeline, host_empty
 
     dist = init_dist(world)
     torch.cuda.set_device(local)
@@ -315,16 +315,20 @@ def run_ours(args, world, rank, local):
         # window.
         n_win = 5
         e2e_steps = max(2, min(args.steps, 30) // n_win)  # steps per window
-        def pinned_copy(t):
-            h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+
+        def host_copy(t):  # huge-page page-locked host memory (ep_host_alloc)
+            h = host_empty(tuple(t.shape), t.dtype)
             h.copy_(t)
             return h
-        x_h, lg_h, ro_h, y_h = (pinned_copy(t) for t in (x, logits, ro, y))
-        outs_h = [torch.empty(N, H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        x_h, lg_h, ro_h, y_h = (host_copy(t) for t in (x, logits, ro, y))
+        outs_h = [host_empty((N, H), torch.bfloat16) for _ in range(2)]
         h2d = x_h.numel() * 2 + lg_h.numel() * 4 + ro_h.numel() * 4 + y_h.numel() * 2
         d2h = outs_h[0].numel() * 2
         hp = HostPipeline(N, E, K, H, R, dtype, dev, cap=cap, expert_map=emap)
         torch.cuda.synchronize()
+
+        def gbs(nbytes, ms):
+            return round(nbytes / ms / 1e6, 1) if ms > 0 else None
 
         def pipelined_window(n):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -336,31 +340,40 @@ def run_ours(args, world, rank, local):
             b.record(stream)
             torch.cuda.synchronize()
             barrier(dist)
-            return max_over_ranks(dist, a.elapsed_time(b))
+            t_in, t_out = hp.copy_ms()  # the window's last step
+            return max_over_ranks(dist, a.elapsed_time(b)), (gbs(h2d, t_in), gbs(d2h, t_out))
 
         def serial_window(n):
-            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(n)]
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
             barrier(dist)
-            for a, b in ev:
-                a.record(stream)
+            for e in ev:
+                e[0].record(stream)
                 x.copy_(x_h, non_blocking=True)
                 logits.copy_(lg_h, non_blocking=True)
                 ro.copy_(ro_h, non_blocking=True)
                 y.copy_(y_h, non_blocking=True)
+                e[1].record(stream)
                 step()
+                e[2].record(stream)
                 outs_h[0].copy_(comb, non_blocking=True)
-                b.record(stream)
+                e[3].record(stream)
             torch.cuda.synchronize()
             barrier(dist)
-            return max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in ev))
+            last = ev[-1]
+            rates = (gbs(h2d, last[0].elapsed_time(last[1])),
+                     gbs(d2h, last[2].elapsed_time(last[3])))
+            return max_over_ranks(dist, sum(e[0].elapsed_time(e[3]) for e in ev)), rates
 
         pipelined_window(2)  # warm-up of both schedules
         serial_window(1)
-        win_pipe, win_serial = [], []
+        win_pipe, win_serial, rate_pipe, rate_serial = [], [], [], []
         for _ in range(n_win):
-            win_pipe.append(pipelined_window(e2e_steps))
-            win_serial.append(serial_window(e2e_steps))
+            t, r = pipelined_window(e2e_steps)
+            win_pipe.append(t)
+            rate_pipe.append(r)
+            t, r = serial_window(e2e_steps)
+            win_serial.append(t)
+            rate_serial.append(r)
         e2e_ms = statistics.median(win_pipe)
         serial_ms = statistics.median(win_serial)
         tok_step = N * world * e2e_steps
@@ -371,14 +384,18 @@ def run_ours(args, world, rank, local):
             "schedule": "ep_host_pipeline_* (C ABI, via pipeline.HostPipeline): step i+1's "
                         "copies in overlap step i's kernels and copy out (double-buffered "
                         "device inputs and result)",
+            "host_memory": "ep_host_alloc: page-locked, transparent-huge-page backed",
             "h2d_GB/s": round(h2d * e2e_steps / (e2e_ms / 1e3) / 1e9, 1),
             "windows": f"{n_win} windows of {e2e_steps} steps, alternating with the "
                        "serial schedule; median window",
             "window_ms_per_step": [round(t / e2e_steps, 3) for t in win_pipe],
+            "window_last_step_copy_GB/s_in_out": rate_pipe,
             "serial": {"value": round(tok_step / (serial_ms / 1e3), 1),
                        "ms_per_step": round(serial_ms / e2e_steps, 3),
                        "window_ms_per_step": [round(t / e2e_steps, 3) for t in win_serial],
+                       "window_last_step_copy_GB/s_in_out": rate_serial,
                        "schedule": "one step alone: copies in, kernels, copy out"}}
+        hp.close()
         del hp, x_h, lg_h, ro_h, y_h, outs_h
 
     # other schedules of the same batch, and the decode step (after the e2e

@@ -61,9 +61,16 @@ def lib():
                                               P, sz, ctypes.POINTER(P)]
         L.ep_host_pipeline_step.argtypes = [P, P, P, P, P, P, P]
         L.ep_host_pipeline_join.argtypes = [P, P]
+        L.ep_host_pipeline_copy_ms.argtypes = [P, ctypes.POINTER(ctypes.c_float),
+                                               ctypes.POINTER(ctypes.c_float)]
+        L.ep_host_pipeline_copy_ms.restype = ctypes.c_int
         L.ep_host_pipeline_buffer.argtypes = [P, ctypes.c_int, ctypes.POINTER(P),
                                               ctypes.POINTER(sz)]
         L.ep_host_pipeline_destroy.argtypes = [P]
+        L.ep_host_alloc.argtypes = [sz, ctypes.POINTER(P)]
+        L.ep_host_alloc.restype = ctypes.c_int
+        L.ep_host_free.argtypes = [P]
+        L.ep_host_free.restype = ctypes.c_int
         for f in ("ep_route_topk", "ep_expert_balance_map", "ep_dispatch_layout", "ep_dispatch",
                   "ep_combine"):
             getattr(L, f).restype = ctypes.c_int

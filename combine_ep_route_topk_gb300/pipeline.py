@@ -28,6 +28,12 @@ HostPipeline
     previous step's kernels and copy out.  The host link, not HBM, bounds
     such a step.
 
+host_empty
+    A CPU tensor in the library's page-locked host memory (ep_host_alloc):
+    huge-page backed, so that the host pipeline's multi-gigabyte copies do
+    not slow down whenever the kernel reactivates the pages of an ordinary
+    pinned buffer.
+
 All only call the C ABI through the binding (every step runs in the
 library's kernels); the host work is slicing and stream ordering.
 """
@@ -231,6 +237,31 @@ def chunked(logits, x, rank_offsets_host, K, dtype, bufs, expert_out, comb, ro_r
     return rounds
 
 
+def host_empty(shape, dtype):
+    """Uninitialised CPU tensor of `shape` and `dtype` in page-locked,
+    huge-page-backed host memory from ep_host_alloc (include/ep.h).  Copies
+    to and from it run asynchronously, like those of torch's pinned memory.
+    The memory returns to the library (ep_host_free) when the last tensor
+    that views it is gone."""
+    import ctypes
+    import math
+    L = _ep.lib()
+    nbytes = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+    ptr = ctypes.c_void_p()
+    _ep._check("ep_host_alloc", L.ep_host_alloc(max(1, nbytes), ctypes.byref(ptr)))
+    addr = ptr.value
+
+    def _free(_self, addr=addr, L=L):
+        L.ep_host_free(ctypes.c_void_p(addr))
+
+    # a ctypes array over the mapping that frees it when collected; the
+    # tensor keeps it alive
+    owner_t = type("HostBytes", (ctypes.c_uint8 * max(1, nbytes),), {"__del__": _free})
+    owner = owner_t.from_address(addr)
+    t = torch.frombuffer(owner, dtype=torch.uint8)[:nbytes]
+    return t.view(dtype).view(shape)
+
+
 class HostPipeline:
     """route -> layout -> dispatch -> combine over host buffers, pipelined:
     the binding of the library's native pipeline (ep_host_pipeline_* in
@@ -326,6 +357,16 @@ class HostPipeline:
         with torch.cuda.device(self.device):
             _ep._check("ep_host_pipeline_join",
                        _ep.lib().ep_host_pipeline_join(self._h, _ep._stream(stream)))
+
+    def copy_ms(self):
+        """(h2d_ms, d2h_ms): device-timed copies in and copy out of the last
+        step, once it is done (after synchronize())."""
+        import ctypes
+        a, b = ctypes.c_float(), ctypes.c_float()
+        with torch.cuda.device(self.device):
+            _ep._check("ep_host_pipeline_copy_ms", _ep.lib().ep_host_pipeline_copy_ms(
+                self._h, ctypes.byref(a), ctypes.byref(b)))
+        return a.value, b.value
 
     def synchronize(self):
         with torch.cuda.device(self.device):

@@ -285,6 +285,36 @@ ep_status_t ep_combine(const void* y, int32_t N, int32_t H, int32_t E, int32_t K
                        void* out, void* stream);
 
 /*
+ * ep_layout_dispatch -- ep_dispatch_layout followed by ep_dispatch, with the
+ * same arguments and bit-identical outputs, as one launch for problems of at
+ * most 16384 picks (N*K; the decode-sized ones).  [Anatomy] "High
+ * throughput: ask first, then send" and "Dispatch"; [SGLang] "Supported
+ * backends" (the low-latency mode).  No block of that launch waits for
+ * another: each counts the expert ids it needs itself (they are at most 64 KB
+ * and are read from L2), so a token's row is stored as soon as its block has
+ * the row's positions, instead of after a layout launch.
+ *   x, H, layout, cap, dtype, out, out_scales   as for ep_dispatch (cap > 0
+ *              for MASKED; for CONTIG, cap > 0 also yields masked_m and
+ *              overflow_count as ep_dispatch_layout does).
+ *   topk_idx, rank_offsets, R, counts ... overflow_count   as for
+ *              ep_dispatch_layout.
+ *   workspace  ep_layout_dispatch_workspace_size bytes: 0 (NULL allowed) for
+ *              problems the one launch serves; above 16384 picks the call
+ *              runs the layout kernels and the dispatch kernel instead and
+ *              needs the layout workspace (EP_ERR_WORKSPACE without it).
+ */
+size_t ep_layout_dispatch_workspace_size(int32_t N, int32_t E, int32_t K, int32_t R);
+
+ep_status_t ep_layout_dispatch(const void* x, const int32_t* topk_idx,
+                               const int32_t* rank_offsets, int32_t R, int32_t N, int32_t H,
+                               int32_t E, int32_t K, ep_layout_t layout, int32_t cap,
+                               ep_dtype_t dtype, int32_t* counts, int32_t* expert_offsets,
+                               int32_t* rank_expert_offsets, int32_t* pos, int32_t* row_src,
+                               int32_t* masked_m, int32_t* overflow_count, void* out,
+                               float* out_scales, void* workspace, size_t ws_bytes,
+                               void* stream);
+
+/*
  * ep_host_pipeline_* -- no counterpart in the source pages: the path for
  * callers whose inputs and results live in host memory.  Each step copies the
  * step's logits, rank offsets, tokens x and expert outputs y in, runs
@@ -303,7 +333,7 @@ ep_status_t ep_combine(const void* y, int32_t N, int32_t H, int32_t E, int32_t K
  *              bytes, 256-byte aligned, owned by the caller and kept alive
  *              (and untouched) until ep_host_pipeline_destroy returns.  Every
  *              device buffer of the pipeline lives in it.
- * The object itself holds three streams and 5*depth + 1 events on the device
+ * The object itself holds three streams and 7*depth + 1 events on the device
  * that was current at creation; call its functions with that device
  * current.
  */
@@ -337,6 +367,14 @@ ep_status_t ep_host_pipeline_step(ep_host_pipeline_t* pipeline, const float* log
 /* Makes `stream` wait for every step enqueued so far. */
 ep_status_t ep_host_pipeline_join(ep_host_pipeline_t* pipeline, void* stream);
 
+/* Device-timed durations, in milliseconds, of the last enqueued step's
+ * copies in (logits, rank offsets, x and y, from the start of the first to
+ * the end of the last) and of its copy out, once that step is done (after a
+ * join and a sync).  EP_ERR_INVALID_ARG before the first step or for NULL
+ * pointers; EP_ERR_CUDA (times 0) while the step is still running. */
+ep_status_t ep_host_pipeline_copy_ms(const ep_host_pipeline_t* pipeline, float* h2d_ms,
+                                     float* d2h_ms);
+
 /* Device buffers of the last step's intermediate outputs, inside the
  * workspace (valid after a join and a sync): the routed picks and weights,
  * the layout, and the dispatched rows (and FP8 scales). */
@@ -360,6 +398,29 @@ ep_status_t ep_host_pipeline_buffer(const ep_host_pipeline_t* pipeline, ep_host_
 /* Waits for the pipeline's streams, then releases its streams and events and
  * the object (NULL is a no-op).  The workspace is the caller's to free. */
 ep_status_t ep_host_pipeline_destroy(ep_host_pipeline_t* pipeline);
+
+/*
+ * ep_host_alloc / ep_host_free -- no counterpart in the source pages: page-
+ * locked host memory for the host pipeline's inputs and results.  The
+ * pipeline's copies stream gigabytes per step over the host link; on a
+ * GB300 machine (64 KB base pages) the kernel's periodic reactivation of the
+ * pages of ordinary pinned buffers (cudaHostAlloc) was measured to cut a
+ * copy that overlapped it from 211 to about 50 GB/s, while copies from
+ * buffers backed by huge pages never slowed.  ep_host_alloc therefore maps
+ * anonymous memory aligned to the huge-page size, asks for transparent huge
+ * pages (madvise), touches it and page-locks it with cudaHostRegister.
+ * Where the kernel offers no transparent huge pages the memory is still
+ * page-locked, on base pages.
+ *   bytes  > 0; rounded up to whole huge pages (a 1-byte buffer holds one).
+ *   *out   receives the host pointer (aligned to the huge-page size), usable
+ *          by the host and by copies on every device; NULL on failure.
+ * Returns EP_ERR_INVALID_ARG for bytes == 0 or out == NULL, EP_ERR_CUDA if
+ * the mapping or the registration fails.  Allocates host memory only.
+ * ep_host_free unregisters and unmaps a pointer from ep_host_alloc (NULL is
+ * a no-op; any other pointer returns EP_ERR_INVALID_ARG).  Thread-safe.
+ */
+ep_status_t ep_host_alloc(size_t bytes, void** out);
+ep_status_t ep_host_free(void* ptr);
 
 /*
  * ep_selftest_wait_timeout -- no counterpart in the source pages: a check of
