@@ -569,9 +569,12 @@ def _time_schedule(args, torch, main_stream, flush, dist, step, N, note):
 
 def decode_latency(args, ep, torch, dev, stream, flush):
     """Latency of one decode step (the low-latency, masked layout): 8 ranks x
-    128 tokens, E=256, K=8, H=7168, capacity 128; route + layout (fused
-    kernel, and as separate kernels), masked bf16 dispatch, masked combine.
-    L2 flushed before every step."""
+    128 tokens, E=256, K=8, H=7168, capacity 128; route, layout, masked bf16
+    dispatch and masked combine, in three arrangements: four separate calls
+    (the layout as one block per expert, the default), the same with the
+    one-cluster layout (EP_LAYOUT_SMALL=0 while the step is captured and
+    launched), and route + layout as the cooperative kernel
+    (ep_route_layout).  L2 flushed before every step."""
     from combine_ep_route_topk_gb300 import workloads as wl
     w = wl.WORKLOADS["decode"]
     inp = wl.make_inputs(w, seed=args.seed + 1, device=str(dev))
@@ -586,20 +589,25 @@ def decode_latency(args, ep, torch, dev, stream, flush):
     out = torch.empty(E * cap, H, dtype=torch.bfloat16, device=dev)
     comb = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
 
-    def step(fused):
-        if fused:
+    def step(kind):
+        if kind == "fused_route_layout":
             ep.ep_route_layout(inp["logits"], inp["rank_offsets"], K, cap, topk_idx=idx,
                                topk_w=wt, out=lay, status=st, workspace=ws)
         else:
             ep.ep_route_topk(inp["logits"], K, topk_idx=idx, topk_w=wt)
-            ep.ep_dispatch_layout(idx, inp["rank_offsets"], E, cap, out=lay, workspace=ws)
-        ep.ep_dispatch(inp["x"], idx, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_MASKED, cap,
-                       out=out)
+            if kind == "cluster_layout":
+                os.environ["EP_LAYOUT_SMALL"] = "0"
+            try:
+                ep.ep_dispatch_layout(idx, inp["rank_offsets"], E, cap, out=lay, workspace=ws)
+            finally:
+                os.environ.pop("EP_LAYOUT_SMALL", None)
+        ep.ep_dispatch(inp["x"], idx, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_MASKED,
+                       cap, out=out)
         ep.ep_combine(inp["y"], idx, wt, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_MASKED,
                       cap, out=comb)
 
     res = {}
-    for fused in (True, False):
+    for fused in ("separate", "cluster_layout", "fused_route_layout"):
         for i in range(3):
             step(fused)
         torch.cuda.synchronize()
@@ -623,7 +631,9 @@ def decode_latency(args, ep, torch, dev, stream, flush):
                 evs[i][1].record(stream)
             torch.cuda.synchronize()
             ts = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
-            key = ("fused" if fused else "separate") + "_route_layout_" + mode
+            key = {"fused_route_layout": "fused_route_layout_",
+                   "cluster_layout": "separate_cluster_layout_",
+                   "separate": "separate_route_layout_"}[fused] + mode
             res[key] = {"us_median": round(ts[n // 2], 2), "us_min": round(ts[0], 2),
                         "tokens_per_s": round(N / (ts[n // 2] / 1e6), 1)}
         del graph

@@ -15,12 +15,12 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libep_gb300.so")
-SOURCES = ["ep_api.cu", "route_topk.cu", "layout.cu", "layout_cluster.cu", "layout_static.cu",
+SOURCES = ["ep_api.cu", "route_topk.cu", "layout.cu", "layout_cluster.cu", "layout_static.cu", "layout_small.cu",
            "host_pipeline.cu",
            "route_layout.cu",
            "dispatch.cu", "combine.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ep_kernels.cuh", "route_common.cuh",
-                                            "layout_common.cuh")] + [
+                                            "layout_common.cuh", "dispatch_common.cuh")] + [
     os.path.join(ROOT, "include", "ep.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

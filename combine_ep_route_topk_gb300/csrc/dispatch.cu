@@ -13,15 +13,12 @@
 // and x/scale use IEEE division, and the E4M3 conversion is the hardware
 // round-to-nearest-even satfinite cvt.  Bytes moved per token:
 // H*2 read + K*(H*b_out + scales) written; the kernel is HBM-bound.
-#include <cuda_bf16.h>
-#include <cuda_fp8.h>
-
-#include "ep_kernels.cuh"
+#include "dispatch_common.cuh"
 
 namespace ep {
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
+using namespace mv;
 
 // Destination row of pick (t, k), or -1 when the pick is not delivered.
 __device__ __forceinline__ long long dest_row(const MoveArgs& a, int t, int k) {
@@ -64,33 +61,6 @@ __global__ void __launch_bounds__(NT) dispatch_bf16_kernel(MoveArgs a) {
     }
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// Two values -> two E4M3 codes, low byte = first value.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
-
-// E4M3 codes of 16 values as 16 bytes (value j in byte j).
-__device__ __forceinline__ uint4 quantize16(const uint4& lo, const uint4& hi, float scale) {
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    uint32_t p[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        p[j] = e4m3x2(__fdiv_rn(bf16_lo(w[j]), scale), __fdiv_rn(bf16_hi(w[j]), scale));
-    return make_uint4(p[0] | (p[1] << 16), p[2] | (p[3] << 16), p[4] | (p[5] << 16),
-                      p[6] | (p[7] << 16));
-}
-
-__device__ __forceinline__ float amax16(const uint4& lo, const uint4& hi) {
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    float m = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
-    return m;
-}
-
 // Each thread owns 16 consecutive values; 8 lanes make one 128-column scale
 // block.  One 16-byte code store per destination, and one scale store per
 // block and destination (lane 0 of the 8).
@@ -125,10 +95,7 @@ __global__ void __launch_bounds__(NT) dispatch_fp8_kernel(MoveArgs a) {
         float sc[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            float amax = amax16(lo[u], hi[u]);
-#pragma unroll
-            for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, off));
-            sc[u] = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+            sc[u] = block_scale(amax16(lo[u], hi[u]));
             q[u] = quantize16(lo[u], hi[u], sc[u]);
         }
         for (int k = 0; k < a.K; ++k) {

@@ -81,9 +81,15 @@ struct LayoutArgs {
     int32_t* ws_totals;  // [E] expert totals
 };
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t s);
-// Small problems: the whole layout in one thread-block cluster (no workspace).
+// Small problems: the whole layout in one launch of one block per expert (no
+// workspace), or in one thread-block cluster.
+bool layout_small_fits(int N, int E, int K, int R);
+cudaError_t launch_layout_small(const LayoutArgs& a, cudaStream_t s);
 bool layout_cluster_fits(int N, int E, int K, int R);
 cudaError_t launch_layout_cluster(const LayoutArgs& a, cudaStream_t s);
+// EP_LAYOUT_CLUSTER=0 in the environment: the three layout kernels for every
+// size (read at every call).
+bool layout_kernels_forced();
 
 // ---- fused route + layout (one cooperative kernel) ------------------------
 int route_layout_chunk_tokens(int N);

@@ -16,8 +16,10 @@
 //              per-warp bases and __match_any_sync ranks, so the result never
 //              depends on atomic ordering.
 // Everything stays on the device (no host read of a count), so the masked
-// decode path can be captured in a CUDA graph.  Problems small enough for one
-// thread-block cluster take the one-launch variant in layout_cluster.cu.
+// decode path can be captured in a CUDA graph.  Problems of at most 16384
+// picks take the one-launch, one-block-per-expert variant in layout_small.cu;
+// layout_cluster.cu holds a one-cluster variant for the same sizes, used when
+// the first is switched off.
 #include "layout_common.cuh"
 
 namespace ep {
@@ -146,6 +148,10 @@ __global__ void __launch_bounds__(kNT) layout_scatter_kernel(LayoutArgs a, int C
 }  // namespace
 
 cudaError_t launch_layout(const LayoutArgs& a, cudaStream_t s) {
+    if (layout_small_fits(a.N, a.E, a.K, a.R)) {  // layout_small.cu
+        note_launch(1);
+        return launch_layout_small(a, s);
+    }
     if (layout_cluster_fits(a.N, a.E, a.K, a.R)) {  // layout_cluster.cu
         note_launch(1);
         return launch_layout_cluster(a, s);

@@ -292,9 +292,13 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kCT)
 // The one-cluster path serves problems of at most kMaxPicks picks and
 // kMaxRanks ranks whose chunk rows fit in shared memory.  EP_LAYOUT_CLUSTER=0 in the environment
 // (read at every call) selects the three-kernel path for every size.
-bool layout_cluster_fits(int N, int E, int K, int R) {
+bool layout_kernels_forced() {
     const char* v = std::getenv("EP_LAYOUT_CLUSTER");
-    if (v && v[0] == '0') return false;
+    return v && v[0] == '0';
+}
+
+bool layout_cluster_fits(int N, int E, int K, int R) {
+    if (layout_kernels_forced()) return false;
     if ((long long)N * K > kMaxPicks || R > kMaxRanks) return false;
     return cluster_plan(N, E, R).smem <= kMaxSmem;
 }

@@ -161,11 +161,13 @@ size_t ep_dispatch_layout_workspace_size(int32_t N, int32_t E, int32_t K, int32_
  * method") matters only to ep_expert_balance_map, which requires E % R == 0.
  * A micro-batch of a subset of the ranks (one rank of eight, say, with all
  * 256 experts) is therefore a valid layout problem.
- * Problems of at most 16384 picks (N*K) and 64 ranks whose chunk rows fit in
- * shared memory run as one launch of one thread-block cluster; larger ones as
- * three kernels.  EP_LAYOUT_CLUSTER=0 in the environment (read at every call)
- * selects the three kernels for every size.  Both give the same results, which
- * are deterministic (no order depends on atomics).
+ * Problems of at most 16384 picks (N*K) run as one launch of one block per
+ * expert (no workspace is touched); larger ones as three kernels.  In the
+ * environment (read at every call) EP_LAYOUT_SMALL=0 switches the first path
+ * off, so that problems of at most 16384 picks and 64 ranks whose chunk rows
+ * fit in shared memory run as one thread-block cluster, and
+ * EP_LAYOUT_CLUSTER=0 selects the three kernels for every size.  All give the
+ * same results, which are deterministic (no order depends on atomics).
  */
 ep_status_t ep_dispatch_layout(const int32_t* topk_idx, const int32_t* rank_offsets,
                                int32_t R, int32_t N, int32_t E, int32_t K, int32_t cap,
@@ -283,36 +285,6 @@ ep_status_t ep_combine(const void* y, int32_t N, int32_t H, int32_t E, int32_t K
                        const int32_t* topk_idx, const float* topk_w, const int32_t* pos,
                        const int32_t* expert_offsets, ep_layout_t layout, int32_t cap,
                        void* out, void* stream);
-
-/*
- * ep_layout_dispatch -- ep_dispatch_layout followed by ep_dispatch, with the
- * same arguments and bit-identical outputs, as one launch for problems of at
- * most 16384 picks (N*K; the decode-sized ones).  [Anatomy] "High
- * throughput: ask first, then send" and "Dispatch"; [SGLang] "Supported
- * backends" (the low-latency mode).  No block of that launch waits for
- * another: each counts the expert ids it needs itself (they are at most 64 KB
- * and are read from L2), so a token's row is stored as soon as its block has
- * the row's positions, instead of after a layout launch.
- *   x, H, layout, cap, dtype, out, out_scales   as for ep_dispatch (cap > 0
- *              for MASKED; for CONTIG, cap > 0 also yields masked_m and
- *              overflow_count as ep_dispatch_layout does).
- *   topk_idx, rank_offsets, R, counts ... overflow_count   as for
- *              ep_dispatch_layout.
- *   workspace  ep_layout_dispatch_workspace_size bytes: 0 (NULL allowed) for
- *              problems the one launch serves; above 16384 picks the call
- *              runs the layout kernels and the dispatch kernel instead and
- *              needs the layout workspace (EP_ERR_WORKSPACE without it).
- */
-size_t ep_layout_dispatch_workspace_size(int32_t N, int32_t E, int32_t K, int32_t R);
-
-ep_status_t ep_layout_dispatch(const void* x, const int32_t* topk_idx,
-                               const int32_t* rank_offsets, int32_t R, int32_t N, int32_t H,
-                               int32_t E, int32_t K, ep_layout_t layout, int32_t cap,
-                               ep_dtype_t dtype, int32_t* counts, int32_t* expert_offsets,
-                               int32_t* rank_expert_offsets, int32_t* pos, int32_t* row_src,
-                               int32_t* masked_m, int32_t* overflow_count, void* out,
-                               float* out_scales, void* workspace, size_t ws_bytes,
-                               void* stream);
 
 /*
  * ep_host_pipeline_* -- no counterpart in the source pages: the path for

@@ -200,3 +200,4 @@ def test_host_memory_argument_checks(L):
     assert L.ep_host_free(p(4096)) == INVALID  # not from ep_host_alloc
     a, b = ctypes.c_float(), ctypes.c_float()
     assert L.ep_host_pipeline_copy_ms(None, ctypes.byref(a), ctypes.byref(b)) == INVALID
+

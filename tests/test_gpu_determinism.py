@@ -35,12 +35,18 @@ def _run(inp, w, layout, cap, dtype, fused):
     return res
 
 
-@pytest.mark.parametrize("name,layout,dtype,fused", [
-    ("prefill", EP_LAYOUT_CONTIG, EP_DTYPE_FP8_E4M3_B128, False),  # three layout kernels
-    ("decode", EP_LAYOUT_MASKED, EP_DTYPE_BF16, False),            # one-cluster layout
-    ("decode", EP_LAYOUT_MASKED, EP_DTYPE_BF16, True),             # cooperative kernel
+@pytest.mark.parametrize("name,layout,dtype,fused,small", [
+    ("prefill", EP_LAYOUT_CONTIG, EP_DTYPE_FP8_E4M3_B128, False, True),  # three layout kernels
+    ("decode", EP_LAYOUT_MASKED, EP_DTYPE_BF16, False, True),    # one block per expert
+    ("decode", EP_LAYOUT_MASKED, EP_DTYPE_BF16, False, False),   # one-cluster layout
+    ("decode", EP_LAYOUT_MASKED, EP_DTYPE_BF16, True, True),     # cooperative kernel
 ])
-def test_hundred_repetitions_are_bit_identical(name, layout, dtype, fused):
+def test_hundred_repetitions_are_bit_identical(name, layout, dtype, fused, small, monkeypatch):
+    monkeypatch.delenv("EP_LAYOUT_CLUSTER", raising=False)
+    if small:
+        monkeypatch.delenv("EP_LAYOUT_SMALL", raising=False)
+    else:
+        monkeypatch.setenv("EP_LAYOUT_SMALL", "0")
     w = wl.WORKLOADS[name]
     if name == "prefill":
         w = w.scaled(batch=("fixed", 600), H=1024)

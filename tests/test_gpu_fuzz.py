@@ -2,8 +2,8 @@
 stage by stage, so that no stage's inputs come from the CUDA path:
   - route: random E, K (E not a multiple of 32, odd K, K = E), ties;
   - layout: random ranks (empty ones, up to 70), capacities, some picks
-    invalid or duplicated within a token, on both layout implementations
-    (one cluster, three kernels);
+    invalid or duplicated within a token, on the three layout implementations
+    (one block per expert, one cluster, three kernels);
   - dispatch: bf16 or FP8 rows, contiguous or masked, from the oracle's layout;
   - combine: from the oracle's weights and layout, bit-exact.
 Sizes are small so that the oracle finishes in seconds."""
@@ -68,11 +68,13 @@ def test_random_configuration(seed, monkeypatch):
 
     # layout of those picks, both implementations
     olay = oracle.layout(oidx, offs, E, cap)
-    for path in ("cluster", "kernels"):
+    for path in ("small", "cluster", "kernels"):
+        monkeypatch.delenv("EP_LAYOUT_CLUSTER", raising=False)
+        monkeypatch.delenv("EP_LAYOUT_SMALL", raising=False)
         if path == "kernels":
             monkeypatch.setenv("EP_LAYOUT_CLUSTER", "0")
-        else:
-            monkeypatch.delenv("EP_LAYOUT_CLUSTER", raising=False)
+        elif path == "cluster":
+            monkeypatch.setenv("EP_LAYOUT_SMALL", "0")
         lay = ep_dispatch_layout(torch.from_numpy(oidx).cuda(), torch.from_numpy(offs).cuda(),
                                  E, cap)
         for name in ("counts", "expert_offsets", "rank_expert_offsets", "pos", "row_src"):
@@ -82,6 +84,7 @@ def test_random_configuration(seed, monkeypatch):
             np.testing.assert_array_equal(np_(lay.masked_m), olay["masked_m"])
             assert int(np_(lay.overflow_count)[0]) == olay["overflow"]
     monkeypatch.delenv("EP_LAYOUT_CLUSTER", raising=False)
+    monkeypatch.delenv("EP_LAYOUT_SMALL", raising=False)
 
     # dispatch from the oracle's layout
     pos_d = torch.from_numpy(olay["pos"]).cuda()

@@ -122,15 +122,20 @@ def test_route_topk_empty_batch():
 
 # ----------------------------------------------------------------- layout ---
 
-@pytest.fixture(params=["cluster", "kernels"])
+@pytest.fixture(params=["small", "cluster", "kernels"])
 def layout_path(request, monkeypatch):
-    """The layout's two implementations: one thread-block cluster (problems up
-    to 16384 picks and 64 ranks whose chunk rows fit in shared memory) and
-    the three kernels (every size; forced with EP_LAYOUT_CLUSTER=0)."""
+    """The layout's three implementations: one block per expert (problems up
+    to 16384 picks, the default there), one thread-block cluster (the same
+    sizes with at most 64 ranks whose chunk rows fit in shared memory, when
+    the first is off: EP_LAYOUT_SMALL=0) and the three kernels (every size;
+    forced with EP_LAYOUT_CLUSTER=0).  Sizes a path does not serve fall to
+    the next one."""
+    monkeypatch.delenv("EP_LAYOUT_CLUSTER", raising=False)
+    monkeypatch.delenv("EP_LAYOUT_SMALL", raising=False)
     if request.param == "kernels":
         monkeypatch.setenv("EP_LAYOUT_CLUSTER", "0")
-    else:
-        monkeypatch.delenv("EP_LAYOUT_CLUSTER", raising=False)
+    elif request.param == "cluster":
+        monkeypatch.setenv("EP_LAYOUT_SMALL", "0")
     return request.param
 
 
@@ -156,7 +161,7 @@ def test_layout_parity(name, seed, layout_path):
     ([1] * 1024, 64, 4, 100),                    # R = 1024
     ([5000, 1, 3000], 256, 8, 64),               # chunks > 32 tokens, ragged
     ([125] * 8, 1024, 8, 16),                    # E = 1024: 90 KB of shared memory per CTA
-    ([64] * 8, 1024, 32, 40),                    # 16384 picks: the largest one-cluster case
+    ([64] * 8, 1024, 32, 40),                    # 16384 picks: the largest one-launch case
     ([2048, 1], 16, 8, 2000),                    # just over it: the three kernels
     ([16] * 64, 64, 4, 3),                       # 64 ranks: the widest one-cluster chunk table
     ([0, 3] * 32 + [5], 32, 2, 1),               # 65 ranks, empty ones: the three kernels
@@ -204,28 +209,32 @@ def test_layout_all_tokens_one_expert_and_invalid_ids(layout_path):
     _check_layout(gpu, ref, cap)
 
 
-@pytest.mark.parametrize("B,E,K,expect", [
-    ([128] * 8, 256, 8, 1),        # the decode shape: one cluster
-    ([64] * 8, 1024, 32, 1),       # 16384 picks
-    ([2048, 1], 16, 8, 3),         # 16392 picks: three kernels
-    ([16] * 64, 64, 4, 1),         # 64 ranks
-    ([16] * 65, 65, 4, 3),         # 65 ranks: three kernels
-    ([4096] * 8, 256, 8, 3),       # the prefill shape
+@pytest.mark.parametrize("B,E,K,small,cluster", [
+    ([128] * 8, 256, 8, 1, 1),        # the decode shape
+    ([64] * 8, 1024, 32, 1, 1),       # 16384 picks
+    ([2048, 1], 16, 8, 3, 3),         # 16392 picks: three kernels
+    ([16] * 64, 64, 4, 1, 1),         # 64 ranks
+    ([16] * 65, 65, 4, 1, 3),         # 65 ranks: too many for one cluster
+    ([1] * 1024, 64, 4, 1, 3),        # 1024 ranks
+    ([4096] * 8, 256, 8, 3, 3),       # the prefill shape
 ])
-def test_layout_path_choice(B, E, K, expect, monkeypatch):
-    """Which implementation serves a size (launches per layout call)."""
+def test_layout_path_choice(B, E, K, small, cluster, monkeypatch):
+    """Which implementation serves a size (launches per layout call): by
+    default, with the one-block-per-expert path off, and with the three
+    kernels forced."""
     from combine_ep_route_topk_gb300 import ep as epb
     monkeypatch.delenv("EP_LAYOUT_CLUSTER", raising=False)
+    monkeypatch.delenv("EP_LAYOUT_SMALL", raising=False)
     N = sum(B)
     offs = torch.tensor(np.concatenate([[0], np.cumsum(B)]), dtype=torch.int32, device="cuda")
     idx = torch.zeros(N, K, dtype=torch.int32, device="cuda")
-    before = epb.lib().ep_kernel_launch_count()
-    ep_dispatch_layout(idx, offs, E)
-    assert epb.lib().ep_kernel_launch_count() - before == expect
-    monkeypatch.setenv("EP_LAYOUT_CLUSTER", "0")
-    before = epb.lib().ep_kernel_launch_count()
-    ep_dispatch_layout(idx, offs, E)
-    assert epb.lib().ep_kernel_launch_count() - before == 3
+    for env, expect in ((None, small), (("EP_LAYOUT_SMALL", "0"), cluster),
+                        (("EP_LAYOUT_CLUSTER", "0"), 3)):
+        if env:
+            monkeypatch.setenv(*env)
+        before = epb.lib().ep_kernel_launch_count()
+        ep_dispatch_layout(idx, offs, E)
+        assert epb.lib().ep_kernel_launch_count() - before == expect, env
     torch.cuda.synchronize()
 
 
@@ -527,7 +536,7 @@ def test_cuda_graph_capture_masked_decode():
         _compare_chain(g, o, w, EP_LAYOUT_MASKED, cap, EP_DTYPE_BF16)
 
 
-@pytest.mark.parametrize("per_rank", [100, 600])  # one-cluster layout / three kernels
+@pytest.mark.parametrize("per_rank", [100, 600])  # one-launch layout / three kernels
 def test_cuda_graph_capture_contiguous_fp8(per_rank):
     """route -> layout -> FP8 contiguous dispatch -> combine captured once in
     a CUDA graph and replayed on new logits, tokens and expert outputs copied

@@ -11,7 +11,7 @@ ep_dispatch_layout (integer outputs, so both comparisons are bit-exact).  The
 array keeps the previous call's contents, which must never leak into the next
 result, so the calls that are compared all take the three-kernel path, the
 one that uses the array (EP_LAYOUT_CLUSTER=0 for the small problems, which
-would otherwise run as one thread-block cluster without scratch).  One case
+would otherwise run as one launch without scratch).  One case
 needs exactly the whole array, so its expert totals end on its last bytes.
 
 This file is collected last on purpose: a failure here stops a -x run only
