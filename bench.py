@@ -606,6 +606,18 @@ def decode_latency(args, ep, torch, dev, stream, flush):
         ep.ep_combine(inp["y"], idx, wt, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_MASKED,
                       cap, out=comb)
 
+    # L2 before each step: the 512 MiB write, then a 512 MiB read pass, so
+    # the step starts with none of its inputs in L2 and with L2 holding clean
+    # lines; with the write alone, the step would also write back up to
+    # 129 MB of the flush's dirty lines, about half of its own traffic (the
+    # default arrangement is timed that way too, for comparison)
+    rd = torch.ones(512 << 20, dtype=torch.uint8, device=dev)
+
+    def flush_l2(i, clean=True):
+        flush.fill_(i & 0xFF)
+        if clean:
+            rd.view(torch.int32).amax()
+
     res = {}
     for fused in ("separate", "cluster_layout", "fused_route_layout"):
         for i in range(3):
@@ -617,14 +629,15 @@ def decode_latency(args, ep, torch, dev, stream, flush):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             step(fused)
-        for mode in ("graph", "eager"):
+        modes = ("graph", "eager", "graph_l2_dirty") if fused == "separate" else ("graph", "eager")
+        for mode in modes:
             n = 100
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(n)]
             for i in range(n):
-                flush.fill_(i & 0xFF)
+                flush_l2(i, clean=mode != "graph_l2_dirty")
                 evs[i][0].record(stream)
-                if mode == "graph":
+                if mode != "eager":
                     graph.replay()
                 else:
                     step(fused)
@@ -640,6 +653,9 @@ def decode_latency(args, ep, torch, dev, stream, flush):
     if int(st.item()) != 0:
         raise RuntimeError("route+layout kernel reported a barrier timeout")
     res["workload"] = "decode: 8 ranks x 128 tokens, E=256, K=8, H=7168, masked cap 128, bf16"
+    res["l2"] = ("before each step: 512 MiB write then 512 MiB read (clean L2, no input "
+                 "resident); *_l2_dirty: the write alone (the step also writes back the "
+                 "flush's dirty lines)")
     return res
 
 

@@ -31,13 +31,42 @@ __device__ __forceinline__ long long dest_row(const MoveArgs& a, int t, int k) {
     return (long long)e * a.cap + slot;
 }
 
+// Destination rows of token t's picks into s_dst.  For the masked layout the
+// expert-offset table is staged in shared memory by the whole block at the
+// same time as the picks are read (one round of global loads, not two).
+// Every thread calls it.
+template <int NT>
+__device__ __forceinline__ void load_dests(const MoveArgs& a, int t, long long* s_dst,
+                                           int* s_eoff) {
+    if (a.layout == 1) {
+        for (int e = threadIdx.x; e < a.E; e += NT) s_eoff[e] = __ldg(a.expert_offsets + e);
+        int p = -1, e = -1;
+        if (threadIdx.x < a.K) {
+            p = __ldg(a.pos + (size_t)t * a.K + threadIdx.x);
+            e = __ldg(a.topk_idx + (size_t)t * a.K + threadIdx.x);
+        }
+        __syncthreads();
+        if (threadIdx.x < a.K) {
+            long long row = -1;
+            if (p >= 0 && e >= 0 && e < a.E) {
+                const int slot = p - s_eoff[e];
+                if (slot >= 0 && slot < a.cap) row = (long long)e * a.cap + slot;
+            }
+            s_dst[threadIdx.x] = row;
+        }
+    } else if (threadIdx.x < a.K) {
+        s_dst[threadIdx.x] = dest_row(a, t, threadIdx.x);
+    }
+    __syncthreads();
+}
+
 template <int NT, int U>
 __global__ void __launch_bounds__(NT) dispatch_bf16_kernel(MoveArgs a) {
     __shared__ long long s_dst[kMaxK];
+    __shared__ int s_eoff[kMaxE];
     pdl_prologue();
     const int t = blockIdx.x;
-    if (threadIdx.x < a.K) s_dst[threadIdx.x] = dest_row(a, t, threadIdx.x);
-    __syncthreads();
+    load_dests<NT>(a, t, s_dst, s_eoff);
     const int V = a.H >> 3;  // 16-byte vectors per row
     const uint4* src = reinterpret_cast<const uint4*>(a.src) + (size_t)t * V;
     uint4* dst = reinterpret_cast<uint4*>(a.dst);
@@ -67,10 +96,10 @@ __global__ void __launch_bounds__(NT) dispatch_bf16_kernel(MoveArgs a) {
 template <int NT, int U>
 __global__ void __launch_bounds__(NT) dispatch_fp8_kernel(MoveArgs a) {
     __shared__ long long s_dst[kMaxK];
+    __shared__ int s_eoff[kMaxE];
     pdl_prologue();
     const int t = blockIdx.x;
-    if (threadIdx.x < a.K) s_dst[threadIdx.x] = dest_row(a, t, threadIdx.x);
-    __syncthreads();
+    load_dests<NT>(a, t, s_dst, s_eoff);
     const int G = a.H >> 4;   // 16-value groups per row; 8 per scale block
     const int SB = a.H >> 7;  // scale blocks per row
     const uint4* src = reinterpret_cast<const uint4*>(a.src) + (size_t)t * (a.H >> 3);

@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(kST, SC <= 16 ? 2 : 1) layout_small_kernel(Lay
         const int i = base + s * 32 + lane;
         v[s] = (s * 32 < span && i < NK) ? __ldg(a.topk_idx + i) : -1;
     }
+    // the first 32 rank offsets, read now so their latency overlaps the ids'
+    const int ro0 = (lane <= R) ? __ldg(a.rank_offsets + lane) : 0;
 
     if (e == E) {  // ---- what belongs to no expert
         int* s_hist = smem;                  // [E]
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(kST, SC <= 16 ? 2 : 1) layout_small_kernel(Lay
     int carry = 0;
     for (int r0 = 0; r0 <= R; r0 += 32) {
         const int r = r0 + lane;
-        int o = (r <= R) ? clamp_tok(__ldg(a.rank_offsets + r), N) : 0;
+        int o = (r <= R) ? clamp_tok(r0 == 0 ? ro0 : __ldg(a.rank_offsets + r), N) : 0;
         o = max(o, carry);
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
