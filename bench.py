@@ -570,11 +570,12 @@ def _time_schedule(args, torch, main_stream, flush, dist, step, N, note):
 def decode_latency(args, ep, torch, dev, stream, flush):
     """Latency of one decode step (the low-latency, masked layout): 8 ranks x
     128 tokens, E=256, K=8, H=7168, capacity 128; route, layout, masked bf16
-    dispatch and masked combine, in three arrangements: four separate calls
-    (the layout as one block per expert, the default), the same with the
+    dispatch and masked combine, in four arrangements: ep_route_dispatch
+    (route, layout and dispatch in two launches) then ep_combine; four
+    separate calls (the layout as one block per expert); the same with the
     one-cluster layout (EP_LAYOUT_SMALL=0 while the step is captured and
-    launched), and route + layout as the cooperative kernel
-    (ep_route_layout).  L2 flushed before every step."""
+    launched); route + layout as the cooperative kernel (ep_route_layout).
+    L2 flushed before every step."""
     from combine_ep_route_topk_gb300 import workloads as wl
     w = wl.WORKLOADS["decode"]
     inp = wl.make_inputs(w, seed=args.seed + 1, device=str(dev))
@@ -589,7 +590,17 @@ def decode_latency(args, ep, torch, dev, stream, flush):
     out = torch.empty(E * cap, H, dtype=torch.bfloat16, device=dev)
     comb = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
 
+    ws_rd = torch.empty(ep.ep_route_dispatch_workspace_size(N, E, K, R), dtype=torch.uint8,
+                        device=dev)
+
     def step(kind):
+        if kind == "route_dispatch":  # ep_route_dispatch: two launches, then combine
+            ep.ep_route_dispatch(inp["logits"], inp["rank_offsets"], inp["x"], K,
+                                 ep.EP_LAYOUT_MASKED, cap, topk_idx=idx, topk_w=wt, lay=lay,
+                                 out=out, workspace=ws_rd)
+            ep.ep_combine(inp["y"], idx, wt, lay.pos, lay.expert_offsets, E, ep.EP_LAYOUT_MASKED,
+                          cap, out=comb)
+            return
         if kind == "fused_route_layout":
             ep.ep_route_layout(inp["logits"], inp["rank_offsets"], K, cap, topk_idx=idx,
                                topk_w=wt, out=lay, status=st, workspace=ws)
@@ -619,7 +630,7 @@ def decode_latency(args, ep, torch, dev, stream, flush):
             rd.view(torch.int32).amax()
 
     res = {}
-    for fused in ("separate", "cluster_layout", "fused_route_layout"):
+    for fused in ("route_dispatch", "separate", "cluster_layout", "fused_route_layout"):
         for i in range(3):
             step(fused)
         torch.cuda.synchronize()
@@ -629,7 +640,8 @@ def decode_latency(args, ep, torch, dev, stream, flush):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             step(fused)
-        modes = ("graph", "eager", "graph_l2_dirty") if fused == "separate" else ("graph", "eager")
+        modes = (("graph", "eager", "graph_l2_dirty") if fused in ("separate", "route_dispatch")
+                 else ("graph", "eager"))
         for mode in modes:
             n = 100
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -644,7 +656,8 @@ def decode_latency(args, ep, torch, dev, stream, flush):
                 evs[i][1].record(stream)
             torch.cuda.synchronize()
             ts = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
-            key = {"fused_route_layout": "fused_route_layout_",
+            key = {"route_dispatch": "route_dispatch_then_combine_",
+                   "fused_route_layout": "fused_route_layout_",
                    "cluster_layout": "separate_cluster_layout_",
                    "separate": "separate_route_layout_"}[fused] + mode
             res[key] = {"us_median": round(ts[n // 2], 2), "us_min": round(ts[0], 2),

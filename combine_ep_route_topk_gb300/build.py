@@ -17,7 +17,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libep_gb300.so")
 SOURCES = ["ep_api.cu", "route_topk.cu", "layout.cu", "layout_cluster.cu", "layout_static.cu", "layout_small.cu",
            "host_pipeline.cu",
-           "route_layout.cu",
+           "route_layout.cu", "route_dispatch.cu",
            "dispatch.cu", "combine.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("ep_kernels.cuh", "route_common.cuh",
                                             "layout_common.cuh", "dispatch_common.cuh")] + [

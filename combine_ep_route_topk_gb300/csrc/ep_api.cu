@@ -276,6 +276,125 @@ ep_status_t ep_combine(const void* y, int32_t N, int32_t H, int32_t E, int32_t K
     return cuda_status(launch_combine(a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t ep_route_dispatch_workspace_size(int32_t N, int32_t E, int32_t K, int32_t R) {
+    if (N < 0) N = 0;
+    if (E < 1) E = 1;
+    if (R < 1) R = 1;
+    if (K < 1) K = 1;
+    size_t b = route_dispatch_fits(N, E, K, R) ? route_dispatch_hist_bytes(N, E)
+                                               : layout_workspace_bytes(N, E, K, R);
+    b = ((b + 255) / 256) * 256;
+    return b > 0 ? b : 256;
+}
+
+ep_status_t ep_route_dispatch(const float* logits, const int32_t* rank_offsets, const void* x,
+                              int32_t R, int32_t N, int32_t H, int32_t E, int32_t K,
+                              const int32_t* expert_map, ep_layout_t layout, int32_t cap,
+                              ep_dtype_t dtype, int32_t* topk_idx, float* topk_w,
+                              int32_t* counts, int32_t* expert_offsets,
+                              int32_t* rank_expert_offsets, int32_t* pos, int32_t* row_src,
+                              int32_t* masked_m, int32_t* overflow_count, void* out,
+                              float* out_scales, void* workspace, size_t ws_bytes,
+                              void* stream) {
+    ep_status_t st = check_sizes(N, E, K);
+    if (st != EP_OK) return st;
+    if (R < 1) return EP_ERR_INVALID_ARG;
+    if (R > kMaxR) return EP_ERR_UNSUPPORTED;
+    if (cap < 0) return EP_ERR_INVALID_ARG;
+    if ((masked_m || overflow_count) && cap == 0) return EP_ERR_INVALID_ARG;
+    if (layout != EP_LAYOUT_CONTIG && layout != EP_LAYOUT_MASKED) return EP_ERR_INVALID_ARG;
+    if (layout == EP_LAYOUT_MASKED && cap < 1) return EP_ERR_INVALID_ARG;
+    if (H < 8 || H % 8 != 0) return EP_ERR_INVALID_ARG;
+    if (dtype != EP_DTYPE_BF16 && dtype != EP_DTYPE_FP8_E4M3_B128) return EP_ERR_INVALID_ARG;
+    if (dtype == EP_DTYPE_FP8_E4M3_B128 && H % 128 != 0) return EP_ERR_INVALID_ARG;
+    if (!rank_offsets || !counts || !expert_offsets || !rank_expert_offsets)
+        return EP_ERR_INVALID_ARG;
+    if (N > 0 && (!logits || !x || !topk_idx || !topk_w || !pos || !row_src || !out))
+        return EP_ERR_INVALID_ARG;
+    if (N > 0 && dtype == EP_DTYPE_FP8_E4M3_B128 && !out_scales) return EP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out)) return EP_ERR_INVALID_ARG;
+    const void* ptrs[] = {logits, rank_offsets, expert_map, topk_idx, topk_w, counts,
+                          expert_offsets, rank_expert_offsets, pos, row_src, masked_m,
+                          overflow_count, out_scales};
+    for (const void* p : ptrs)
+        if (!aligned4(p)) return EP_ERR_INVALID_ARG;
+    const size_t need = ep_route_dispatch_workspace_size(N, E, K, R);
+    if (!workspace || ws_bytes < need || !aligned16(workspace)) return EP_ERR_WORKSPACE;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (route_dispatch_fits(N, E, K, R)) {
+        int32_t* hist = static_cast<int32_t*>(workspace);
+        cudaError_t err = cudaSuccess;
+        if (N > 0)
+            err = launch_route_hist(logits, N, E, K, expert_map, topk_idx, topk_w, hist,
+                                    cap > 0 ? overflow_count : nullptr, s);
+        else if (overflow_count)
+            err = cudaMemsetAsync(overflow_count, 0, sizeof(int32_t), s);
+        if (err != cudaSuccess) return cuda_status(err);
+        RouteDispatchArgs a;
+        a.topk_idx = topk_idx;
+        a.rank_offsets = rank_offsets;
+        a.hist = hist;
+        a.R = R;
+        a.N = N;
+        a.E = E;
+        a.K = K;
+        a.H = H;
+        a.cap = cap;
+        a.C = route_chunks(N);
+        a.layout = (int)layout;
+        a.dtype = (int)dtype;
+        a.counts = counts;
+        a.expert_offsets = expert_offsets;
+        a.rank_expert_offsets = rank_expert_offsets;
+        a.pos = pos;
+        a.row_src = row_src;
+        a.masked_m = masked_m;
+        a.overflow = overflow_count;
+        a.x = x;
+        a.out = out;
+        a.scales = out_scales;
+        return cuda_status(launch_route_dispatch(a, s));
+    }
+    // larger problems: the route kernel, the layout kernels, the dispatch kernel
+    cudaError_t err = launch_route_topk(logits, N, E, K, expert_map, topk_idx, topk_w, s);
+    if (err != cudaSuccess) return cuda_status(err);
+    LayoutArgs l;
+    l.topk_idx = topk_idx;
+    l.rank_offsets = rank_offsets;
+    l.R = R;
+    l.N = N;
+    l.E = E;
+    l.K = K;
+    l.cap = cap;
+    l.counts = counts;
+    l.expert_offsets = expert_offsets;
+    l.rank_expert_offsets = rank_expert_offsets;
+    l.pos = pos;
+    l.row_src = row_src;
+    l.masked_m = masked_m;
+    l.overflow = overflow_count;
+    l.ws_hist = static_cast<int32_t*>(workspace);
+    l.ws_totals = l.ws_hist + (size_t)layout_chunk_slots(N, R) * E;
+    err = launch_layout(l, s);
+    if (err != cudaSuccess) return cuda_status(err);
+    MoveArgs m;
+    m.src = x;
+    m.dst = out;
+    m.scales = out_scales;
+    m.topk_idx = topk_idx;
+    m.topk_w = nullptr;
+    m.pos = pos;
+    m.expert_offsets = expert_offsets;
+    m.N = N;
+    m.H = H;
+    m.E = E;
+    m.K = K;
+    m.cap = cap;
+    m.layout = (int)layout;
+    m.dtype = (int)dtype;
+    return cuda_status(launch_dispatch(m, s));
+}
+
 ep_status_t ep_selftest_wait_timeout(int32_t* status, void* workspace, size_t ws_bytes,
                                      void* stream) {
     if (!status || !workspace || ws_bytes < sizeof(unsigned)) return EP_ERR_INVALID_ARG;

@@ -56,6 +56,19 @@ void note_launch(int n = 1);
 cudaError_t launch_route_topk(const float* logits, int N, int E, int K, const int32_t* emap,
                               int32_t* topk_idx, float* topk_w, cudaStream_t s);
 
+// Tokens routed per block of the route kernels (one warp each).
+constexpr int kRouteTokensPerBlock = 8;
+__host__ __device__ inline int route_chunks(int N) {
+    return (N + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+}
+// Route, plus per-block expert histograms H [E][C] and their exclusive
+// prefixes over experts P [E][C] in hist (C = route_chunks(N); expert-major,
+// so one expert's values over all blocks are contiguous); zeroes *zero_me
+// (may be null).
+cudaError_t launch_route_hist(const float* logits, int N, int E, int K, const int32_t* emap,
+                              int32_t* topk_idx, float* topk_w, int32_t* hist,
+                              int32_t* zero_me, cudaStream_t s);
+
 cudaError_t launch_balance_map(const int32_t* counts, int R, int E, int32_t* emap,
                                cudaStream_t s);
 
@@ -127,5 +140,30 @@ struct MoveArgs {
 };
 cudaError_t launch_dispatch(const MoveArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const MoveArgs& a, cudaStream_t s);
+
+// ---- layout + dispatch after route_hist (ep_route_dispatch) ---------------
+constexpr int kRouteDispatchMaxTokens = 2048;
+struct RouteDispatchArgs {
+    const int32_t* topk_idx;
+    const int32_t* rank_offsets;
+    const int32_t* hist;        // H [E][C], then P [E][C], from launch_route_hist
+    int R, N, E, K, H, cap, C;
+    int layout;                 // 0 contiguous, 1 masked
+    int dtype;                  // 0 bf16, 1 fp8 e4m3 1x128
+    int32_t* counts;
+    int32_t* expert_offsets;
+    int32_t* rank_expert_offsets;
+    int32_t* pos;
+    int32_t* row_src;
+    int32_t* masked_m;
+    int32_t* overflow;          // zeroed by launch_route_hist
+    const void* x;
+    void* out;
+    float* scales;
+};
+// Sizes served by the two launches (at most 2048 tokens and 16384 picks).
+bool route_dispatch_fits(int N, int E, int K, int R);
+size_t route_dispatch_hist_bytes(int N, int E);
+cudaError_t launch_route_dispatch(const RouteDispatchArgs& a, cudaStream_t s);
 
 }  // namespace ep

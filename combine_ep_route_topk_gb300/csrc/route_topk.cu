@@ -1,7 +1,9 @@
 // Route top-K and balanced expert renumbering for sm_103a.
 //
 // route_topk: one warp per token runs route::route_token (route_common.cuh);
-// HBM-bound on the N*E*4 logit bytes, issue-bound at small E.
+// HBM-bound on the N*E*4 logit bytes, issue-bound at small E.  route_hist:
+// the same, plus each block's expert histogram and its prefix, for
+// ep_route_dispatch.
 //
 // balance_map: "21K output tokens/s DeepSeek inference on AMD Instinct MI300X
 // GPUs with Expert Parallelism", "Load balancing across GPUs" -- renumber
@@ -11,6 +13,7 @@
 #include <climits>
 
 #include "ep_kernels.cuh"
+#include "layout_common.cuh"
 #include "route_common.cuh"
 
 namespace ep {
@@ -35,6 +38,70 @@ route_topk_kernel(const float* __restrict__ logits, int N, int E, int Kr,
     if (lane < K) {
         topk_idx[(size_t)t * K + lane] = id;
         topk_w[(size_t)t * K + lane] = w;
+    }
+}
+
+// Route + the block's expert histogram, for ep_route_dispatch: block b routes
+// tokens 8b .. 8b+7 (one warp each, as route_topk_kernel does) and writes
+// H[e][b] (its picks of expert e) and P[e][b] (their exclusive prefix over
+// experts) for every e, so that a later kernel can place any pick from these
+// columns alone.  Block 0 zeroes *zero_me (the overflow counter that kernel
+// accumulates into).
+template <int VPL, bool VEC, int KT>
+__global__ void __launch_bounds__(256)
+route_hist_kernel(const float* __restrict__ logits, int N, int E, int Kr,
+                  const int32_t* __restrict__ emap, int32_t* __restrict__ topk_idx,
+                  float* __restrict__ topk_w, int32_t* __restrict__ hist, int C,
+                  int32_t* zero_me) {
+    __shared__ int s_h[kMaxE];
+    __shared__ int s_tmp[32];
+    pdl_prologue();
+    const int K = KT > 0 ? KT : Kr;
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kRouteTokensPerBlock + (threadIdx.x >> 5);
+    for (int e = threadIdx.x; e < E; e += 256) s_h[e] = 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && zero_me) *zero_me = 0;
+    __syncthreads();
+    if (t < N) {  // warp-uniform
+        int id;
+        float w;
+        route::route_token<VPL, VEC, KT>(logits + (size_t)t * E, E, Kr, emap, lane, id, w);
+        if (lane < K) {
+            topk_idx[(size_t)t * K + lane] = id;
+            topk_w[(size_t)t * K + lane] = w;
+            if (id >= 0) atomicAdd(s_h + id, 1);  // route_token returns -1 or an id < E
+        }
+    }
+    __syncthreads();
+    // expert-major: H[e][b] at hist[e * C + b], P[e][b] at hist[(E + e) * C + b],
+    // so that a reader of one expert's column over all blocks loads it whole
+    int h[kMaxE / 256];
+#pragma unroll
+    for (int j = 0; j < kMaxE / 256; ++j) {
+        const int e = threadIdx.x + j * 256;
+        h[j] = (e < E) ? s_h[e] : 0;
+        if (e < E) hist[(size_t)e * C + blockIdx.x] = h[j];
+    }
+    __syncthreads();
+    lay::block_scan_inplace<256, false>(s_h, E, s_tmp);  // inclusive
+#pragma unroll
+    for (int j = 0; j < kMaxE / 256; ++j) {
+        const int e = threadIdx.x + j * 256;
+        if (e < E) hist[((size_t)E + e) * C + blockIdx.x] = s_h[e] - h[j];
+    }
+}
+
+template <int VPL, bool VEC>
+cudaError_t launch_hist(const float* logits, int N, int E, int K, const int32_t* emap,
+                        int32_t* idx, float* w, int32_t* hist, int32_t* zero_me,
+                        cudaStream_t s) {
+    const int C = route_chunks(N);
+    const dim3 grid(C > 0 ? C : 1), block(256);
+    switch (K) {
+        case 2: return launch(route_hist_kernel<VPL, VEC, 2>, grid, block, 0, s, logits, N, E, K, emap, idx, w, hist, C, zero_me);
+        case 4: return launch(route_hist_kernel<VPL, VEC, 4>, grid, block, 0, s, logits, N, E, K, emap, idx, w, hist, C, zero_me);
+        case 8: return launch(route_hist_kernel<VPL, VEC, 8>, grid, block, 0, s, logits, N, E, K, emap, idx, w, hist, C, zero_me);
+        default: return launch(route_hist_kernel<VPL, VEC, 0>, grid, block, 0, s, logits, N, E, K, emap, idx, w, hist, C, zero_me);
     }
 }
 
@@ -150,6 +217,25 @@ cudaError_t launch_route_topk(const float* logits, int N, int E, int K, const in
     else if (E <= 256) err = launch_route<8, false>(logits, N, E, K, emap, idx, w, s);
     else if (E <= 512) err = launch_route<16, false>(logits, N, E, K, emap, idx, w, s);
     else err = launch_route<32, false>(logits, N, E, K, emap, idx, w, s);
+    note_launch();
+    return err;
+}
+
+cudaError_t launch_route_hist(const float* logits, int N, int E, int K, const int32_t* emap,
+                              int32_t* idx, float* w, int32_t* hist, int32_t* zero_me,
+                              cudaStream_t s) {
+    const bool vec = (E % 128 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
+    cudaError_t err;
+    if (vec && E == 128) err = launch_hist<4, true>(logits, N, E, K, emap, idx, w, hist, zero_me, s);
+    else if (vec && E == 256) err = launch_hist<8, true>(logits, N, E, K, emap, idx, w, hist, zero_me, s);
+    else if (vec && E == 512) err = launch_hist<16, true>(logits, N, E, K, emap, idx, w, hist, zero_me, s);
+    else if (vec && E == 1024) err = launch_hist<32, true>(logits, N, E, K, emap, idx, w, hist, zero_me, s);
+    else if (E <= 32) err = launch_hist<1, false>(logits, N, E, K, emap, idx, w, hist, zero_me, s);
+    else if (E <= 64) err = launch_hist<2, false>(logits, N, E, K, emap, idx, w, hist, zero_me, s);
+    else if (E <= 128) err = launch_hist<4, false>(logits, N, E, K, emap, idx, w, hist, zero_me, s);
+    else if (E <= 256) err = launch_hist<8, false>(logits, N, E, K, emap, idx, w, hist, zero_me, s);
+    else if (E <= 512) err = launch_hist<16, false>(logits, N, E, K, emap, idx, w, hist, zero_me, s);
+    else err = launch_hist<32, false>(logits, N, E, K, emap, idx, w, hist, zero_me, s);
     note_launch();
     return err;
 }

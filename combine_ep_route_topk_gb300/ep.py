@@ -54,6 +54,11 @@ def lib():
                                   P, P, P]
         L.ep_combine.argtypes = [P, i32, i32, i32, i32, P, P, P, P, ctypes.c_int, i32, P, P]
         L.ep_selftest_wait_timeout.argtypes = [P, P, sz, P]
+        L.ep_route_dispatch_workspace_size.argtypes = [i32, i32, i32, i32]
+        L.ep_route_dispatch_workspace_size.restype = sz
+        L.ep_route_dispatch.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, ctypes.c_int, i32,
+                                        ctypes.c_int, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
+        L.ep_route_dispatch.restype = ctypes.c_int
         L.ep_host_pipeline_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32,
                                                       ctypes.c_int, i32]
         L.ep_host_pipeline_workspace_size.restype = sz
@@ -222,6 +227,62 @@ def ep_route_layout(logits, rank_offsets, K, cap=0, expert_map=None, topk_idx=No
         _opt(status, torch.int32, "status", (1,)),
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
     return topk_idx, topk_w, out
+
+
+def ep_route_dispatch_workspace_size(N, E, K, R) -> int:
+    return int(lib().ep_route_dispatch_workspace_size(N, E, K, R))
+
+
+def ep_route_dispatch(logits, rank_offsets, x, K, layout=EP_LAYOUT_CONTIG, cap=0,
+                      dtype=EP_DTYPE_BF16, expert_map=None, topk_idx=None, topk_w=None,
+                      lay: Layout | None = None, out=None, out_scales=None, workspace=None,
+                      stream=None):
+    """ep_route_topk + ep_dispatch_layout + ep_dispatch in one call (two
+    launches up to 2048 tokens and 16384 picks).  Returns (topk_idx, topk_w,
+    Layout, out, out_scales) as the three calls would."""
+    N, E = logits.shape
+    H = x.shape[1]
+    R = rank_offsets.shape[0] - 1
+    if topk_idx is None:
+        topk_idx = _empty((N, K), torch.int32, logits)
+    if topk_w is None:
+        topk_w = _empty((N, K), torch.float32, logits)
+    if lay is None:
+        lay = alloc_layout(N, E, K, R, cap, logits.device)
+    rows = dispatch_rows(N, K, E, layout, cap)
+    if dtype == EP_DTYPE_BF16:
+        if out is None:
+            out = _empty((rows, H), torch.bfloat16, x)
+        po = _dev(out, torch.bfloat16, "out")
+    else:
+        if out is None:
+            out = _empty((rows, H), torch.uint8, x)
+        if out_scales is None:
+            out_scales = _empty((rows, H // 128), torch.float32, x)
+        po = _dev(out, torch.uint8, "out")
+    if out.numel() != rows * H:
+        raise EPError(f"out must hold {rows} x {H} elements")
+    if out_scales is not None and out_scales.numel() != rows * (H // 128):
+        raise EPError(f"out_scales must hold {rows} x {H // 128} elements")
+    if workspace is None:
+        workspace = torch.empty(ep_route_dispatch_workspace_size(N, E, K, R), dtype=torch.uint8,
+                                device=logits.device)
+    _check("ep_route_dispatch", lib().ep_route_dispatch(
+        _dev(logits, torch.float32, "logits"), _dev(rank_offsets, torch.int32, "rank_offsets"),
+        _dev(x, torch.bfloat16, "x"), R, N, H, E, K,
+        _opt(expert_map, torch.int32, "expert_map", (E,)), layout, cap, dtype,
+        _dev(topk_idx, torch.int32, "topk_idx", (N, K)),
+        _dev(topk_w, torch.float32, "topk_w", (N, K)),
+        _dev(lay.counts, torch.int32, "counts", (R, E)),
+        _dev(lay.expert_offsets, torch.int32, "expert_offsets", (E + 1,)),
+        _dev(lay.rank_expert_offsets, torch.int32, "rank_expert_offsets", (R, E)),
+        _dev(lay.pos, torch.int32, "pos", (N, K)),
+        _dev(lay.row_src, torch.int32, "row_src", (N * K,)),
+        _opt(lay.masked_m, torch.int32, "masked_m", (E,)),
+        _opt(lay.overflow_count, torch.int32, "overflow_count", (1,)), po,
+        _opt(out_scales, torch.float32, "out_scales"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+    return topk_idx, topk_w, lay, out, out_scales
 
 
 def dispatch_rows(N, K, E, layout, cap):

@@ -287,6 +287,38 @@ ep_status_t ep_combine(const void* y, int32_t N, int32_t H, int32_t E, int32_t K
                        void* out, void* stream);
 
 /*
+ * ep_route_dispatch -- ep_route_topk, ep_dispatch_layout and ep_dispatch in
+ * one call, with the same arguments and bit-identical outputs; problems of at
+ * most 2048 tokens and 16384 picks (the decode-sized ones) take two launches.
+ * [Anatomy] "What we have to do", "High throughput: ask first, then send"
+ * and "Dispatch"; [SGLang] "Supported backends" (the low-latency mode).  The
+ * routing kernel also writes, for each block of 8 tokens, its expert
+ * histogram and the histogram's prefix over experts (into the workspace);
+ * from those rows alone one more kernel places every pick, writes every
+ * layout output and stores the rows, with no layout launch in between.
+ * Larger problems run the route kernel, the layout kernels and the dispatch
+ * kernel, with the same results.
+ *   logits, expert_map, topk_idx, topk_w   as for ep_route_topk.
+ *   rank_offsets, R, cap, counts ... overflow_count   as for
+ *              ep_dispatch_layout (overflow_count is zeroed by the call).
+ *   x, H, layout, dtype, out, out_scales   as for ep_dispatch (cap > 0 for
+ *              MASKED).
+ *   workspace  ep_route_dispatch_workspace_size bytes, 16-byte aligned, no
+ *              initialisation needed (EP_ERR_WORKSPACE otherwise).
+ */
+size_t ep_route_dispatch_workspace_size(int32_t N, int32_t E, int32_t K, int32_t R);
+
+ep_status_t ep_route_dispatch(const float* logits, const int32_t* rank_offsets, const void* x,
+                              int32_t R, int32_t N, int32_t H, int32_t E, int32_t K,
+                              const int32_t* expert_map, ep_layout_t layout, int32_t cap,
+                              ep_dtype_t dtype, int32_t* topk_idx, float* topk_w,
+                              int32_t* counts, int32_t* expert_offsets,
+                              int32_t* rank_expert_offsets, int32_t* pos, int32_t* row_src,
+                              int32_t* masked_m, int32_t* overflow_count, void* out,
+                              float* out_scales, void* workspace, size_t ws_bytes,
+                              void* stream);
+
+/*
  * ep_host_pipeline_* -- no counterpart in the source pages: the path for
  * callers whose inputs and results live in host memory.  Each step copies the
  * step's logits, rank offsets, tokens x and expert outputs y in, runs

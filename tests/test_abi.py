@@ -201,3 +201,30 @@ def test_host_memory_argument_checks(L):
     a, b = ctypes.c_float(), ctypes.c_float()
     assert L.ep_host_pipeline_copy_ms(None, ctypes.byref(a), ctypes.byref(b)) == INVALID
 
+
+
+def test_route_dispatch_argument_checks(L):
+    launches0 = L.ep_kernel_launch_count()
+    f = L.ep_route_dispatch
+    need = L.ep_route_dispatch_workspace_size(100, 16, 2, 4)
+    assert need > 0 and need % 256 == 0
+
+    def call(N=100, H=256, E=16, K=2, R=4, layout=0, cap=0, dtype=0, x=p(), out=p(), sc=p(),
+             mm=None, ov=None, ws=p(), wsb=need):
+        return f(p(), p(), x, R, N, H, E, K, None, layout, cap, dtype, p(), p(), p(), p(), p(),
+                 p(), p(), mm, ov, out, sc, ws, wsb, None)
+    assert call(K=20) == INVALID                 # K > E
+    assert call(layout=1, cap=0) == INVALID      # masked needs a capacity
+    assert call(cap=0, ov=p()) == INVALID        # masked outputs need a capacity
+    assert call(H=100) == INVALID                # H % 8
+    assert call(dtype=1, H=200) == INVALID       # FP8 needs H % 128
+    assert call(dtype=1, sc=None) == INVALID     # FP8 needs scales
+    assert call(x=p(4104)) == INVALID            # x not 16-byte aligned
+    assert call(R=0) == INVALID
+    assert call(R=2000) == UNSUPPORTED
+    assert call(ws=None) == WORKSPACE
+    assert call(wsb=need - 1) == WORKSPACE
+    # past 2048 tokens the layout workspace is needed instead of the histograms
+    big = L.ep_route_dispatch_workspace_size(4096, 16, 2, 4)
+    assert big >= ep.ep_dispatch_layout_workspace_size(4096, 16, 2, 4)
+    assert L.ep_kernel_launch_count() == launches0
