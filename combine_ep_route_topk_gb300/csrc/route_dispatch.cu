@@ -9,6 +9,7 @@
 // P[e][c], expert-major.  These columns are all that is needed to place any
 // pick, so one more kernel does the whole layout and the row copies, with no
 // block waiting for another:
+//   token blocks t (N of them, first in the grid): see below.
 //   expert blocks e (E of them): the column H[e][.] scanned over the blocks
 //       gives e's picks before any token boundary (plus the few ids of a
 //       partial block), hence counts[r][e] and rank_expert_offsets[r][e];
@@ -16,7 +17,7 @@
 //       added to the counter the routing kernel zeroed.
 //   one totals block: expert_offsets[E] (the valid picks) and the -1 tail of
 //       row_src.
-//   token blocks t (N of them): issue the loads of the token's row first,
+//   token blocks t: issue the loads of the token's row first,
 //       then for each pick (t, k) of expert e:
 //           slot = sum_{c < t/8} H[e][c] + #{e's picks in t's block before (t, k)}
 //           pos  = sum_c P[e][c] + slot       (the stable counting sort's answer)
@@ -111,18 +112,14 @@ __device__ void totals_part(const RouteDispatchArgs& a, int* smem) {
 // Token t's positions: pos, row_src, and the destination row of each pick in
 // s_dst (-1: not delivered).  Every thread calls it.
 template <int NT>
-__device__ void token_layout(const RouteDispatchArgs& a, int t, int* s_e, long long* s_dst) {
+__device__ void token_layout(const RouteDispatchArgs& a, int t, long long* s_dst) {
     const int C = a.C, E = a.E, K = a.K;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c0 = t / kRouteTokensPerBlock;
     const int i0 = c0 * kRouteTokensPerBlock * K;  // first id of t's routing block
-    if (threadIdx.x < K) {
-        const int e = __ldg(a.topk_idx + (size_t)t * K + threadIdx.x);
-        s_e[threadIdx.x] = (e >= 0 && e < E) ? e : -1;
-    }
-    __syncthreads();
     for (int k = warp; k < K; k += NT / 32) {  // a warp per pick
-        const int e = s_e[k];
+        int e = __ldg(a.topk_idx + (size_t)t * K + k);  // the same address in every lane
+        if (e < 0 || e >= E) e = -1;
         int before = 0, eo = 0, in = 0;
         if (e >= 0) {
             const int* H = a.hist + (size_t)e * C;        // contiguous over blocks
@@ -156,17 +153,14 @@ template <int NT, int U>
 __global__ void __launch_bounds__(NT) route_dispatch_bf16_kernel(RouteDispatchArgs a) {
     extern __shared__ int smem[];
     __shared__ long long s_dst[kMaxK];
-    __shared__ int s_e[kMaxK];
     pdl_prologue();
-    if ((int)blockIdx.x < a.E) {
-        expert_part<NT>(a, blockIdx.x, smem);
+    if ((int)blockIdx.x >= a.N) {  // after the token blocks, which are on the critical path
+        const int b = (int)blockIdx.x - a.N;
+        if (b < a.E) expert_part<NT>(a, b, smem);
+        else totals_part<NT>(a, smem);
         return;
     }
-    if ((int)blockIdx.x == a.E) {
-        totals_part<NT>(a, smem);
-        return;
-    }
-    const int t = (int)blockIdx.x - a.E - 1;
+    const int t = blockIdx.x;
     const int V = a.H >> 3;  // 16-byte vectors per row
     const uint4* src = reinterpret_cast<const uint4*>(a.x) + (size_t)t * V;
     uint4* dst = reinterpret_cast<uint4*>(a.out);
@@ -176,7 +170,7 @@ __global__ void __launch_bounds__(NT) route_dispatch_bf16_kernel(RouteDispatchAr
         const int c = threadIdx.x + u * NT;
         if (c < V) v[u] = __ldcs(src + c);
     }
-    token_layout<NT>(a, t, s_e, s_dst);
+    token_layout<NT>(a, t, s_dst);
     for (int c0 = threadIdx.x; c0 < V; c0 += NT * U) {
         if (c0 != (int)threadIdx.x) {
 #pragma unroll
@@ -202,17 +196,14 @@ template <int NT, int U>
 __global__ void __launch_bounds__(NT) route_dispatch_fp8_kernel(RouteDispatchArgs a) {
     extern __shared__ int smem[];
     __shared__ long long s_dst[kMaxK];
-    __shared__ int s_e[kMaxK];
     pdl_prologue();
-    if ((int)blockIdx.x < a.E) {
-        expert_part<NT>(a, blockIdx.x, smem);
+    if ((int)blockIdx.x >= a.N) {  // after the token blocks, which are on the critical path
+        const int b = (int)blockIdx.x - a.N;
+        if (b < a.E) expert_part<NT>(a, b, smem);
+        else totals_part<NT>(a, smem);
         return;
     }
-    if ((int)blockIdx.x == a.E) {
-        totals_part<NT>(a, smem);
-        return;
-    }
-    const int t = (int)blockIdx.x - a.E - 1;
+    const int t = blockIdx.x;
     const int G = a.H >> 4;   // 16-value groups per row; 8 per scale block
     const int SB = a.H >> 7;  // scale blocks per row
     const uint4* src = reinterpret_cast<const uint4*>(a.x) + (size_t)t * (a.H >> 3);
@@ -234,7 +225,7 @@ __global__ void __launch_bounds__(NT) route_dispatch_fp8_kernel(RouteDispatchArg
         }
     };
     load(threadIdx.x);
-    token_layout<NT>(a, t, s_e, s_dst);
+    token_layout<NT>(a, t, s_dst);
     // warp-uniform trip count: every lane takes part in the 8-lane shuffles
     for (int g0 = threadIdx.x; g0 - lane < G; g0 += NT * U) {
         if (g0 != (int)threadIdx.x) load(g0);

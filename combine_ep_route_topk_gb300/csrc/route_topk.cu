@@ -13,7 +13,6 @@
 #include <climits>
 
 #include "ep_kernels.cuh"
-#include "layout_common.cuh"
 #include "route_common.cuh"
 
 namespace ep {
@@ -74,20 +73,34 @@ route_hist_kernel(const float* __restrict__ logits, int N, int E, int Kr,
     }
     __syncthreads();
     // expert-major: H[e][b] at hist[e * C + b], P[e][b] at hist[(E + e) * C + b],
-    // so that a reader of one expert's column over all blocks loads it whole
-    int h[kMaxE / 256];
+    // so that a reader of one expert's column over all blocks loads it whole.
+    // Thread j owns experts 4j .. 4j+3: their exclusive prefix is its local
+    // prefix plus a warp scan of the threads' sums plus the earlier warps'.
+    constexpr int kPer = kMaxE / 256;
+    int h[kPer], sum = 0;
 #pragma unroll
-    for (int j = 0; j < kMaxE / 256; ++j) {
-        const int e = threadIdx.x + j * 256;
+    for (int j = 0; j < kPer; ++j) {
+        const int e = threadIdx.x * kPer + j;
         h[j] = (e < E) ? s_h[e] : 0;
         if (e < E) hist[(size_t)e * C + blockIdx.x] = h[j];
+        sum += h[j];
     }
-    __syncthreads();
-    lay::block_scan_inplace<256, false>(s_h, E, s_tmp);  // inclusive
+    int incl = sum;
 #pragma unroll
-    for (int j = 0; j < kMaxE / 256; ++j) {
-        const int e = threadIdx.x + j * 256;
-        if (e < E) hist[((size_t)E + e) * C + blockIdx.x] = s_h[e] - h[j];
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFull, incl, off);
+        if (lane >= off) incl += o;
+    }
+    const int warp = threadIdx.x >> 5;
+    if (lane == 31) s_tmp[warp] = incl;
+    __syncthreads();
+    int run = incl - sum;
+    for (int w = 0; w < warp; ++w) run += s_tmp[w];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int e = threadIdx.x * kPer + j;
+        if (e < E) hist[((size_t)E + e) * C + blockIdx.x] = run;
+        run += h[j];
     }
 }
 
