@@ -465,6 +465,11 @@ def run_ours(args, world, rank, local):
         "roofline": {"kernel": "combine", "bound": "hbm", "achieved": round(comb_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(comb_gbs / peak, 4),
                      "peak_source": peak_kind, "traffic": traffic,
+                     "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum per launch "
+                                     "from a stored ncu capture of this kernel source "
+                                     "(profiles/ncu_traffic.json: 16384 tokens, scaled by 2 "
+                                     "to 32768), not measured in this run; null once the "
+                                     "source has changed since the capture",
                      "algorithmic_bytes": bm["combine"]},
         "dispatch_combine": {"tokens_per_s": round(tok * steps / (dc_ms / 1e3), 1),
                              "ms": round(dc_per, 4),

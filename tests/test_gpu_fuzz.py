@@ -191,3 +191,68 @@ def test_random_balance_map_and_expert_map(seed):
     oidx, ow = oracle.route_topk(logits.numpy(), K, expert_map=emap)
     np.testing.assert_array_equal(np_(idx), oidx)
     np.testing.assert_allclose(np_(w), ow, rtol=weight_rtol())
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_random_route_dispatch(seed):
+    """ep_route_dispatch (two launches up to 2048 tokens and 16384 picks,
+    else route + layout + dispatch) on random sizes, layouts, dtypes and
+    expert maps (some entries out of range), against the oracle's route,
+    layout and dispatch: every output bit-exact, weights within tolerance."""
+    from combine_ep_route_topk_gb300 import ep_route_dispatch
+    rng = np.random.default_rng(11000 + seed)
+    K = int(rng.integers(1, 17))
+    E = int(rng.choice([128, 256, 512])) if rng.random() < 0.5 else int(rng.integers(K, 300))
+    E = max(E, K)
+    R = int(rng.integers(1, 40))
+    B = rng.integers(0, 3000 // R + 1, size=R)  # up to about 3000 tokens: both sides of 2048
+    B[rng.random(R) < 0.2] = 0
+    N = int(B.sum())
+    offs = np.concatenate([[0], np.cumsum(B)]).astype(np.int32)
+    fp8 = rng.random() < 0.4
+    H = int(rng.choice([128, 256])) if fp8 else 8 * int(rng.integers(1, 40))
+    masked = rng.random() < 0.5
+    cap = int(rng.integers(1, 3 * max(1, N * K // E) + 2)) if masked else \
+        (int(rng.integers(1, 8)) if rng.random() < 0.3 else 0)
+    layout = EP_LAYOUT_MASKED if masked else EP_LAYOUT_CONTIG
+    dtype = EP_DTYPE_FP8_E4M3_B128 if fp8 else EP_DTYPE_BF16
+    emap = None
+    if rng.random() < 0.3:
+        emap = rng.permutation(E).astype(np.int32)
+        emap[rng.random(E) < 0.05] = -1
+    g = torch.Generator().manual_seed(11000 + seed)
+    logits = torch.randn(N, E, generator=g)
+    if rng.random() < 0.3:
+        logits = torch.round(logits * 2) / 2
+    x = (torch.randn(N, H, generator=g) * 4).to(torch.bfloat16)
+
+    idx, w, lay, out, sc = ep_route_dispatch(
+        logits.cuda(), torch.from_numpy(offs).cuda(), x.cuda(), K, layout, cap, dtype,
+        expert_map=None if emap is None else torch.from_numpy(emap).cuda())
+    torch.cuda.synchronize()
+    oidx, ow = oracle.route_topk(logits.numpy(), K, expert_map=emap) if N else \
+        (np.zeros((0, K), np.int32), np.zeros((0, K), np.float32))
+    np.testing.assert_array_equal(np_(idx), oidx)
+    np.testing.assert_allclose(np_(w), ow, rtol=weight_rtol())
+    olay = oracle.layout(oidx, offs, E, cap)
+    for name in ("counts", "expert_offsets", "rank_expert_offsets", "pos", "row_src"):
+        np.testing.assert_array_equal(np_(getattr(lay, name)), olay[name], err_msg=name)
+    if cap:
+        np.testing.assert_array_equal(np_(lay.masked_m), olay["masked_m"])
+        assert int(np_(lay.overflow_count)[0]) == olay["overflow"]
+    oout, osc = oracle.dispatch(bits(x), oidx, olay["pos"], olay["expert_offsets"], E,
+                                layout=layout, cap=cap, dtype=dtype)
+    got = bits(out) if dtype == EP_DTYPE_BF16 else np_(out)
+    if masked:  # rows past masked_m are unspecified
+        gm, om = got.reshape(E, cap, H), oout.reshape(E, cap, H)
+        for e in range(E):
+            m = olay["masked_m"][e]
+            np.testing.assert_array_equal(gm[e, :m], om[e, :m])
+            if fp8:
+                np.testing.assert_array_equal(np_(sc).reshape(E, cap, -1)[e, :m],
+                                              osc.reshape(E, cap, -1)[e, :m])
+    else:  # rows past the valid picks are not written
+        nv = olay["expert_offsets"][E]
+        np.testing.assert_array_equal(got[:nv], oout[:nv])
+        if fp8:
+            np.testing.assert_array_equal(np_(sc)[:nv], osc[:nv])
