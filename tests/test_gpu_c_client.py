@@ -1,9 +1,10 @@
 """A plain C program drives the whole path through the C ABI: it reads a
-batch from files, allocates a device workspace and pinned host buffers with
-the CUDA runtime, runs the host-buffer pipeline (ep_host_pipeline_*) for
-three steps and writes every step's combined result.  Each must equal, bit
-for bit, the same batch run through the Python binding; the batch's top-K
-picks are checked against the oracle."""
+batch from files, allocates a device workspace with the CUDA runtime and its
+result buffer with ep_host_alloc, runs the host-buffer pipeline
+(ep_host_pipeline_*) for three steps and writes every step's combined result.
+Each must match the CPU oracle's combine of the same batch (within the
+whole-path bound, each side with its own gate weights) and equal, bit for
+bit, the same batch run through the Python binding."""
 import os
 import subprocess
 
@@ -50,8 +51,8 @@ int main(int argc, char** argv) {
     int* ro = (int*)read_file(dir, "ro.bin", (size_t)(R + 1) * 4);
     void* x = read_file(dir, "x.bin", (size_t)N * H * 2);
     void* y = read_file(dir, "y.bin", rows * H * 2);
-    void* out = NULL;
-    if (cudaMallocHost(&out, (size_t)steps * N * H * 2) != cudaSuccess) return 11;
+    void* out = NULL;  /* the library's huge-page-backed page-locked host memory */
+    if (ep_host_alloc((size_t)steps * N * H * 2, &out) != EP_OK) return 11;
     size_t ws_bytes = ep_host_pipeline_workspace_size(N, E, K, H, R, 0, EP_DTYPE_BF16, 2);
     void* ws = NULL;
     if (ws_bytes == 0 || cudaMalloc(&ws, ws_bytes) != cudaSuccess) return 12;
@@ -75,7 +76,7 @@ int main(int argc, char** argv) {
         return 18;
     fclose(f);
     cudaFree(ws);
-    cudaFreeHost(out);
+    if (ep_host_free(out) != EP_OK) return 19;
     printf("ok %llu kernels\n", (unsigned long long)ep_kernel_launch_count());
     return 0;
 }
@@ -111,5 +112,13 @@ def test_c_program_runs_the_path_through_the_c_abi(tmp_path):
     ref = bits(comb)
     for i in range(steps):
         np.testing.assert_array_equal(got[i], ref)
-    oidx, _ = oracle.route_topk(inp["logits"].numpy(), K)
+    oidx, ow = oracle.route_topk(inp["logits"].numpy(), K)
     np.testing.assert_array_equal(np_(idx), oidx)
+    olay = oracle.layout(oidx, inp["rank_offsets"].numpy(), E)
+    o = dict(idx=oidx, w=ow, lay=olay, y=bits(inp["y"]),
+             comb=oracle.combine(bits(inp["y"]), oidx, ow, olay["pos"], olay["expert_offsets"],
+                                 E))
+    from test_gpu_pipeline import _assert_matches_oracle
+    for i in range(steps):
+        _assert_matches_oracle(torch.from_numpy(got[i].view(np.int16)).view(torch.bfloat16),
+                               o, K, E)
