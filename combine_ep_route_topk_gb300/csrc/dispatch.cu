@@ -13,6 +13,15 @@
 // and x/scale use IEEE division, and the E4M3 conversion is the hardware
 // round-to-nearest-even satfinite cvt.  Bytes moved per token:
 // H*2 read + K*(H*b_out + scales) written; the kernel is HBM-bound.
+//
+// From 4096 tokens on, the row (bf16) or its codes (FP8) are staged in shared
+// memory and each destination row is written by one bulk shared-to-global
+// copy (cp.async.bulk, L2 evict-first), issued by one thread per pick; the
+// FP8 scales stay plain stores.  With fewer tokens the threads store the rows
+// themselves: there the grid is about one wave and the staging barrier costs
+// more than the bulk copies save.
+#include <cstdlib>
+
 #include "dispatch_common.cuh"
 
 namespace ep {
@@ -144,13 +153,126 @@ __global__ void __launch_bounds__(NT) dispatch_fp8_kernel(MoveArgs a) {
     }
 }
 
+// One bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from shared to global memory, with an L2 evict-first hint: the rows are
+// streamed out like the threads' __stcs stores.
+__device__ __forceinline__ void bulk_store_row(void* gdst, const void* ssrc, unsigned bytes) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(ssrc);
+    unsigned long long pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+                 :: "l"(gdst), "r"(sa), "r"(bytes), "l"(pol) : "memory");
+}
+
+// Commit this thread's bulk copies and wait until they have completed (the
+// rows are written, and shared memory may be released).
+__device__ __forceinline__ void bulk_commit_and_wait() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// The threads' shared-memory writes, made visible to the bulk copies, and
+// then thread k < K writes destination row k from s_row.
+__device__ __forceinline__ void bulk_store_dests(const long long* s_dst, int K, void* dst,
+                                                 size_t row_bytes, const void* s_row) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if ((int)threadIdx.x < K) {
+        const long long row = s_dst[threadIdx.x];
+        if (row >= 0) {
+            bulk_store_row(static_cast<unsigned char*>(dst) + row * row_bytes, s_row,
+                           (unsigned)row_bytes);
+            bulk_commit_and_wait();
+        }
+    }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) dispatch_bf16_bulk_kernel(MoveArgs a) {
+    extern __shared__ __align__(128) unsigned char s_row[];  // H * 2 bytes
+    __shared__ long long s_dst[kMaxK];
+    __shared__ int s_eoff[kMaxE];
+    pdl_prologue();
+    const int t = blockIdx.x;
+    load_dests<NT>(a, t, s_dst, s_eoff);
+    const int V = a.H >> 3;
+    const uint4* src = reinterpret_cast<const uint4*>(a.src) + (size_t)t * V;
+    uint4* sr = reinterpret_cast<uint4*>(s_row);
+    for (int c = threadIdx.x; c < V; c += NT) sr[c] = __ldcs(src + c);
+    bulk_store_dests(s_dst, a.K, a.dst, (size_t)V * 16, s_row);
+}
+
+template <int NT, int U>
+__global__ void __launch_bounds__(NT) dispatch_fp8_bulk_kernel(MoveArgs a) {
+    extern __shared__ __align__(128) unsigned char s_codes[];  // H bytes
+    __shared__ long long s_dst[kMaxK];
+    __shared__ int s_eoff[kMaxE];
+    pdl_prologue();
+    const int t = blockIdx.x;
+    load_dests<NT>(a, t, s_dst, s_eoff);
+    const int G = a.H >> 4;
+    const int SB = a.H >> 7;
+    const uint4* src = reinterpret_cast<const uint4*>(a.src) + (size_t)t * (a.H >> 3);
+    uint4* sq = reinterpret_cast<uint4*>(s_codes);
+    const int lane = threadIdx.x & 31;
+    const bool lead = (lane & 7) == 0;
+    // warp-uniform trip count: every lane takes part in the 8-lane shuffles
+    for (int g0 = threadIdx.x; g0 - lane < G; g0 += NT * U) {
+        uint4 lo[U], hi[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int g = g0 + u * NT;
+            if (g < G) {
+                lo[u] = __ldcs(src + 2 * g);
+                hi[u] = __ldcs(src + 2 * g + 1);
+            } else {
+                lo[u] = make_uint4(0, 0, 0, 0);
+                hi[u] = lo[u];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int g = g0 + u * NT;
+            const float sc = block_scale(amax16(lo[u], hi[u]));
+            const uint4 q = quantize16(lo[u], hi[u], sc);
+            if (g < G) {
+                sq[g] = q;
+                if (lead)
+                    for (int k = 0; k < a.K; ++k) {
+                        const long long row = s_dst[k];
+                        if (row >= 0) __stcs(a.scales + row * SB + (g >> 3), sc);
+                    }
+            }
+        }
+    }
+    bulk_store_dests(s_dst, a.K, a.dst, (size_t)a.H, s_codes);
+}
+
+constexpr int kDispatchBulkFrom = 4096;           // tokens
+constexpr size_t kDispatchBulkMaxRow = 32768;     // staged bytes per block
+
+// EP_DISPATCH_BULK=0 in the environment (read at every call) keeps the
+// thread-store kernels at every size.
+bool dispatch_bulk(const MoveArgs& a) {
+    const char* v = std::getenv("EP_DISPATCH_BULK");
+    if (v && v[0] == '0') return false;
+    const size_t row = a.dtype == 0 ? (size_t)a.H * 2 : (size_t)a.H;
+    return a.N >= kDispatchBulkFrom && row <= kDispatchBulkMaxRow &&
+           (reinterpret_cast<uintptr_t>(a.dst) & 15u) == 0;
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const MoveArgs& a, cudaStream_t s) {
     if (a.N == 0) return cudaSuccess;
-    const cudaError_t err =
-        a.dtype == 0 ? launch(dispatch_bf16_kernel<128, 8>, dim3(a.N), dim3(128), 0, s, a)
-                     : launch(dispatch_fp8_kernel<256, 2>, dim3(a.N), dim3(256), 0, s, a);
+    cudaError_t err;
+    if (dispatch_bulk(a))
+        err = a.dtype == 0
+                  ? launch(dispatch_bf16_bulk_kernel<128>, dim3(a.N), dim3(128), (size_t)a.H * 2, s, a)
+                  : launch(dispatch_fp8_bulk_kernel<256, 2>, dim3(a.N), dim3(256), (size_t)a.H, s, a);
+    else
+        err = a.dtype == 0 ? launch(dispatch_bf16_kernel<128, 8>, dim3(a.N), dim3(128), 0, s, a)
+                           : launch(dispatch_fp8_kernel<256, 2>, dim3(a.N), dim3(256), 0, s, a);
     note_launch();
     return err;
 }

@@ -264,6 +264,10 @@ ep_status_t ep_dispatch_layout_static(const int32_t* topk_idx, const int32_t* ra
  *                  [rows, H/128].  The codes are computed once per token and
  *                  written to all K rows.
  *   out            16-byte aligned.
+ * From 4096 tokens on (rows of at most 32 KB), each destination row is written
+ * by one bulk shared-to-global copy; EP_DISPATCH_BULK=0 in the environment
+ * (read at every call) keeps the per-thread stores at every size.  The
+ * results are the same either way.
  */
 ep_status_t ep_dispatch(const void* x, int32_t N, int32_t H, int32_t E, int32_t K,
                         const int32_t* topk_idx, const int32_t* pos,
