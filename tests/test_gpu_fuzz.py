@@ -6,7 +6,8 @@ stage by stage, so that no stage's inputs come from the CUDA path:
     (one block per expert, one cluster, three kernels);
   - dispatch: bf16 or FP8 rows, contiguous or masked, from the oracle's layout;
   - combine: from the oracle's weights and layout, bit-exact.
-Sizes are small so that the oracle finishes in seconds."""
+Sizes are small so that the oracle finishes in seconds, except for the
+dispatch cases at 4096 to 6000 tokens (the bulk-copy kernels)."""
 import numpy as np
 import pytest
 import torch
@@ -256,3 +257,52 @@ def test_random_route_dispatch(seed):
         np.testing.assert_array_equal(got[:nv], oout[:nv])
         if fp8:
             np.testing.assert_array_equal(np_(sc)[:nv], osc[:nv])
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_bulk_dispatch(seed):
+    """Dispatch at 4096 to 6000 tokens, where each destination row leaves
+    shared memory in one bulk copy: random E, K, H, ranks, capacity, bf16 or
+    FP8, some picks invalid or duplicated, from the oracle's layout, against
+    the oracle's rows (and scales)."""
+    rng = np.random.default_rng(9000 + seed)
+    K = int(rng.integers(1, 17))
+    E = int(rng.integers(K, 300))
+    R = int(rng.integers(1, 17))
+    N = int(rng.integers(4096, 6001))
+    cuts = np.sort(rng.integers(0, N + 1, size=R - 1))
+    offs = np.concatenate([[0], cuts, [N]]).astype(np.int32)
+    fp8 = rng.random() < 0.5
+    H = 128 * int(rng.integers(1, 9)) if fp8 else 8 * int(rng.integers(1, 257))
+    masked = rng.random() < 0.4
+    cap = int(rng.integers(1, 2 * N * K // E + 2)) if masked else 0
+    layout = EP_LAYOUT_MASKED if masked else EP_LAYOUT_CONTIG
+    dtype = EP_DTYPE_FP8_E4M3_B128 if fp8 else EP_DTYPE_BF16
+    g = torch.Generator().manual_seed(9500 + seed)
+    oidx, _ = oracle.route_topk(torch.randn(N, E, generator=g).numpy(), K)
+    if rng.random() < 0.35:
+        oidx = oidx.copy()
+        hit = rng.random(oidx.shape) < 0.05
+        oidx[hit] = rng.choice(np.array([-1, E], np.int32), size=int(hit.sum()))
+    x = (torch.randn(N, H, generator=g) * 4).to(torch.bfloat16)
+    olay = oracle.layout(oidx, offs, E, cap)
+    oout, osc = oracle.dispatch(bits(x), oidx, olay["pos"], olay["expert_offsets"], E,
+                                layout=layout, cap=cap, dtype=dtype)
+    out, sc = ep_dispatch(x.cuda(), torch.from_numpy(oidx).cuda(),
+                          torch.from_numpy(olay["pos"]).cuda(),
+                          torch.from_numpy(olay["expert_offsets"]).cuda(), E, layout, cap, dtype)
+    got = bits(out) if dtype == EP_DTYPE_BF16 else np_(out)
+    if masked:  # rows past masked_m are unspecified
+        gm, om = got.reshape(E, cap, H), oout.reshape(E, cap, H)
+        for e in range(E):
+            m = olay["masked_m"][e]
+            np.testing.assert_array_equal(gm[e, :m], om[e, :m])
+            if fp8:
+                np.testing.assert_array_equal(
+                    np_(sc).reshape(E, cap, -1)[e, :m].view(np.uint32),
+                    osc.reshape(E, cap, -1)[e, :m].view(np.uint32))
+    else:
+        n = int(olay["expert_offsets"][E])
+        np.testing.assert_array_equal(got[:n], oout[:n])
+        if fp8:
+            np.testing.assert_array_equal(np_(sc)[:n].view(np.uint32), osc[:n].view(np.uint32))
