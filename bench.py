@@ -436,6 +436,8 @@ def run_ours(args, world, rank, local):
     # the committed counters describe the full-size launch only
     full = not args.tokens_per_rank and args.workload == "prefill"
     traffic = ncu_traffic("combine", ["combine.cu"]) if full else None
+    if full:  # the same kind of stored record for the FP8 dispatch launch
+        kernels["dispatch"]["traffic"] = ncu_traffic("dispatch", ["dispatch.cu"])
     line = {
         "metric": METRIC,
         "value": round(value, 1),
