@@ -636,6 +636,39 @@ def decode_latency(args, ep, torch, dev, stream, flush):
         if clean:
             rd.view(torch.int32).amax()
 
+    def graph_loop(step, flush_l2, m=20, replays=5):
+        """Steps as a model's own graph would hold them: m of them captured
+        in one graph, each after a clean L2 flush, with event-record nodes
+        around each step, so that no step pays for a graph launch.  None
+        when events cannot be recorded inside a graph here."""
+        try:
+            evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True)) for _ in range(m)]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(m):
+                    flush_l2(i)
+                    evs[i][0].record(stream)
+                    step("route_dispatch")
+                    evs[i][1].record(stream)
+            ts = []
+            for r in range(replays + 1):
+                g.replay()
+                torch.cuda.synchronize()
+                if r:  # the first replay warms up
+                    ts += [a.elapsed_time(b) * 1e3 for a, b in evs]
+            del g
+        except (RuntimeError, TypeError):
+            return None
+        ts.sort()
+        mean = statistics.fmean(ts)
+        return {"us_median": round(ts[len(ts) // 2], 2), "us_mean": round(mean, 2),
+                "us_min": round(ts[0], 2), "tokens_per_s": round(N / (mean / 1e6), 1),
+                "steps": len(ts),
+                "how": f"{m} steps in one CUDA graph, each after the clean L2 flush, "
+                       "timed by event-record nodes around the step (no graph launch "
+                       "per step)"}
+
     res = {}
     for fused in ("route_dispatch", "separate", "cluster_layout", "fused_route_layout"):
         for i in range(3):
@@ -674,6 +707,8 @@ def decode_latency(args, ep, torch, dev, stream, flush):
                         "us_min": round(ts[0], 2),
                         "tokens_per_s": round(N / (mean / 1e6), 1)}
         del graph
+        if fused == "route_dispatch":
+            res["route_dispatch_then_combine_graph_loop"] = graph_loop(step, flush_l2)
     if int(st.item()) != 0:
         raise RuntimeError("route+layout kernel reported a barrier timeout")
     res["workload"] = "decode: 8 ranks x 128 tokens, E=256, K=8, H=7168, masked cap 128, bf16"
