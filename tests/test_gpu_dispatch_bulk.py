@@ -80,6 +80,9 @@ def _check(x, idx, lay, E, layout, cap, dtype, monkeypatch):
     ([3000, 1097], 16, 2, 8, CONTIG, 0, BF16),                       # 16-byte rows
     ([2048, 2048], 32, 2, 16384, CONTIG, 0, BF16),                  # 32 KB rows: the staging limit
     ([4096], 8, 2, 16384, MASKED, 900, FP8),                         # 16 KB codes, drops
+    ([4096], 1024, 32, 256, CONTIG, 0, BF16),                       # K = 32 copies per token, E = 1024
+    ([4096], 64, 4, 512, MASKED, 1, FP8),                           # capacity 1: almost all dropped
+    ([2000, 2096], 4, 4, 32896, CONTIG, 0, FP8),                    # 32,896-byte codes: thread stores
 ])
 def test_bulk_dispatch_matches_oracle_and_thread_stores(B, E, K, H, layout, cap, dtype,
                                                         monkeypatch):
