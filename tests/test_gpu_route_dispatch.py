@@ -135,7 +135,8 @@ def test_route_dispatch_expert_map_with_out_of_range_entries():
 
 
 @pytest.mark.parametrize("B,K", [([1000, 1049], 8),     # 2049 tokens
-                                 ([500, 500, 600], 16)])  # 1600 tokens but 25600 picks
+                                 ([500, 500, 600], 16),   # 1600 tokens but 25600 picks
+                                 ([2000, 2100], 4)])      # 4100 tokens: bulk-copy dispatch
 def test_route_dispatch_past_the_limits(B, K):
     """Past 2048 tokens or 16384 picks the call runs the route kernel, the
     layout kernels and the dispatch kernel, with the same results."""
