@@ -4,7 +4,8 @@ configuration, inputs drawn on the device), checked against the oracle:
 routing and layout on every token (the oracle finishes those in about a
 second), FP8 dispatch rows and combine outputs on a sample of tokens that
 the oracle recomputes one by one (random tokens plus the first and last
-token of every rank)."""
+token of every rank).  The end-to-end schedule over host buffers must give
+the device path's results bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -96,3 +97,33 @@ def test_fullsize_combine_sampled_tokens(prefill):
     T = (np.abs(p["ow"][s].astype(np.float64))[..., None] * yf).sum(1)
     bound = bf16_ulp(of) + (weight_rtol() + 2 * K * 2.0 ** -24) * T
     assert np.all(np.abs(gf - of) <= bound * 1.0001)
+
+
+def test_fullsize_host_pipeline_equals_device_path(prefill):
+    """The bench's end-to-end schedule at full size: HostPipeline steps over
+    page-locked huge-page host buffers (ep_host_alloc), copies overlapped
+    across steps.  Its results equal the device path's (checked above against
+    the oracle on sampled tokens) bit for bit, as do its dispatched FP8 rows
+    and layout."""
+    from combine_ep_route_topk_gb300 import pipeline as pl
+    p = prefill
+    w, inp = p["w"], p["inp"]
+    N, E, K, H, R = inp["N"], w.E, w.K, w.H, w.R
+
+    def host(t):
+        h = pl.host_empty(tuple(t.shape), t.dtype)
+        h.copy_(t)
+        return h
+    x_h, lg_h, ro_h, y_h = (host(inp[k]) for k in ("x", "logits", "rank_offsets", "y"))
+    outs = [pl.host_empty((N, H), torch.bfloat16) for _ in range(2)]
+    hp = pl.HostPipeline(N, E, K, H, R, ep.EP_DTYPE_FP8_E4M3_B128)
+    for out_h in outs:
+        hp.step(x_h, lg_h, ro_h, y_h, out_h)
+    hp.synchronize()
+    comb = p["comb"].cpu()
+    for out_h in outs:
+        assert torch.equal(out_h, comb)
+    assert torch.equal(hp.out, p["q"])
+    assert torch.equal(hp.scales, p["qs"])
+    for name in ("counts", "expert_offsets", "pos", "row_src"):
+        assert torch.equal(getattr(hp.layout, name), getattr(p["lay"], name)), name
