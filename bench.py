@@ -428,6 +428,12 @@ def run_ours(args, world, rank, local):
         kernels[k] = {"ms": round(mean[k], 4), "bytes": bm[k], "GB/s": round(gbs, 1),
                       "frac_of_measured": round(gbs / peak, 4),
                       "frac_of_8TBs": round(gbs / SPEC_HBM_GBS, 4)}
+    # what bounds each kernel (ncu summaries in profiles/): routing is integer
+    # compare-and-select work in the ALU pipe, the layout kernels are latency
+    bounds = {"route": "alu", "layout": "latency", "route_layout": "alu",
+              "dispatch": "hbm", "combine": "hbm"}
+    for k in kernels:
+        kernels[k]["bound"] = bounds[k]
     kernels["dispatch"]["GB/s_rowwise_accounting"] = round(
         bm["dispatch_rowwise"] / (mean["dispatch"] / 1e3) / 1e9, 1)
     dc_bytes = bm["dispatch"] + bm["combine"]
